@@ -1,0 +1,409 @@
+#!/usr/bin/env python3
+"""Benchmark of the mHC projection/RMS backward on GB300.
+
+One step = one backward (both kernels) over the training-profile workload
+(T=4096 tokens, K = 4 streams x hidden 5120 = 20480), synthetic seeded inputs
+already resident in HBM.  The metric is achieved HBM bandwidth: algorithmic
+bytes (read X, write dX, read W, write dW, read the 24 used grad_proj columns,
+read r and grad_r) divided by the step time measured with CUDA events on the
+launching stream; L2 is flushed (a 256 MiB write) before every timed step,
+outside the timed interval.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica on its own GPU: the stage has no exchange step (the per-rank dW is
+the caller's to combine), so there is no collective on the data path; ranks
+only meet at barriers and for the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rms_backward_gb300 import workloads as WL  # noqa: E402
+
+METRIC = "mHC proj-bwd µs and achieved HBM GB/s (% of GB300 peak) at T=4096, K=20480"
+WORKLOAD = "training_profile"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--kernel", choices=["tcgen05", "fma"], default="tcgen05")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle timing
+def _oracle_rate(wl_full_T, K, seconds, seed=1):
+    """Runs the CPU oracle on 512-token slices of the training-profile workload
+    until about `seconds` have passed; returns (GB/s-equivalent, tokens, secs)."""
+    sys.path.insert(0, ROOT)
+    import oracle.mhcpb_oracle as O
+    done_tokens, elapsed, nbytes = 0, 0.0, 0
+    piece = 512
+    i = 0
+    while elapsed < seconds and done_tokens < wl_full_T:
+        wl = WL.make("cpu_sample", T=piece, K=K, seed=seed + 1000 * i)
+        t0 = time.perf_counter()
+        O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
+        elapsed += time.perf_counter() - t0
+        done_tokens += piece
+        nbytes += WL.algorithmic_bytes(piece, K)
+        i += 1
+    return nbytes / elapsed / 1e9, done_tokens, elapsed
+
+
+def _cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        blas = [d["num_threads"] for d in info if d.get("user_api") == "blas"]
+        if blas:
+            return int(max(blas))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step runs it on a bounded slice of
+    the training-profile workload, sized so the whole run stays within a few
+    minutes."""
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import oracle.mhcpb_oracle as O
+    T, K = WL.CONFIGS[WORKLOAD]["T"], WL.CONFIGS[WORKLOAD]["K"]
+    # calibrate tokens per step against a ~120 s budget for warmup + steps
+    probe = WL.make("ref_probe", T=64, K=K, seed=77)
+    t0 = time.perf_counter()
+    O.mhc_proj_rms_backward(probe.x, probe.w, probe.grad_proj, probe.grad_r, probe.r)
+    per_token = (time.perf_counter() - t0) / 64
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    tok = int(max(1, min(T, budget / max(per_token, 1e-9))))
+    wl = WL.make("ref_step", T=tok, K=K, seed=78)
+    for _ in range(args.warmup):
+        O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
+    secs = time.perf_counter() - t0
+    gbs = WL.algorithmic_bytes(tok, K) * args.steps / secs / 1e9
+    cores = _cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"training profile T={T} K={K} (4 streams x hidden 5120)",
+                   "T": T, "K": K, "sample_tokens_per_step": tok},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{tok} tokens x K={K} of the training profile per step"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rms_backward_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(kernel):
+    """DRAM bytes per launch of the streaming kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel)
+        if ent and ent.get("source_hash") == _kernel_source_hash():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = _dist_env()
+    if world != args.gpus:
+        if rank == 0:
+            print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from rms_backward_gb300 import Plan, abi
+
+    cfg = WL.CONFIGS[WORKLOAD]
+    T, K = cfg["T"], cfg["K"]
+    wl = WL.make(WORKLOAD, T=T, K=K, seed=cfg["seed"] + 97 * rank)
+    plan = Plan(T, K, local, fma_kernel=(args.kernel == "fma"))
+
+    pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
+    h_x = pin(wl.x.view(np.int16)).view(torch.bfloat16)
+    h_w, h_gp, h_gr, h_r = pin(wl.w), pin(wl.grad_proj), pin(wl.grad_r), pin(wl.r)
+    x = h_x.to(dev)
+    w, gp, gr, r = h_w.to(dev), h_gp.to(dev), h_gr.to(dev), h_r.to(dev)
+    dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((24, K), dtype=torch.float32, device=dev)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step():
+        abi.mhcpb_execute(plan.handle, x.data_ptr(), w.data_ptr(), gp.data_ptr(), gr.data_ptr(),
+                          r.data_ptr(), dx.data_ptr(), dw.data_ptr(), ws.data_ptr(),
+                          plan.workspace_bytes, None, sh)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if plan.device_status() != 0:
+        raise RuntimeError("device-side timeout during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i & 7))
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    if plan.device_status() != 0:
+        raise RuntimeError("device-side timeout during the timed steps")
+    mean_ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([mean_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+
+    alg = WL.algorithmic_bytes(T, K)
+    value = world * alg / (mean_ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+
+    # dominant kernel (the streaming kernel) timed alone: events around each kernel
+    lib = abi.load()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    k1, k2 = [], []
+    for i in range(min(200, args.steps)):
+        flush.fill_(1.0)
+        e0.record(stream)
+        st = lib.mhcpb_execute_profiled(
+            plan.handle, x.data_ptr(), w.data_ptr(), gp.data_ptr(), gr.data_ptr(), r.data_ptr(),
+            dx.data_ptr(), dw.data_ptr(), ws.data_ptr(), plan.workspace_bytes, None, sh,
+            e0.cuda_event, e1.cuda_event, e2.cuda_event)
+        if st != 0:
+            raise RuntimeError(f"mhcpb_execute_profiled: {abi.status_string(st)}")
+        e2.synchronize()
+        k1.append(e0.elapsed_time(e1))
+        k2.append(e1.elapsed_time(e2))
+    k1_ms, k2_ms = float(np.mean(k1)), float(np.mean(k2))
+    k1_bytes = alg - 96 * K          # everything but the dW write, which kernel 2 does
+    k1_gbs = k1_bytes / (k1_ms * 1e-3) / 1e9
+
+    # end to end through the public call with host buffers: H2D of the inputs,
+    # the backward, D2H of dX and dW, every step
+    h_dx = torch.empty((T, K), dtype=torch.bfloat16).pin_memory()
+    h_dw = torch.empty((24, K), dtype=torch.float32).pin_memory()
+    h2d = x.numel() * 2 + w.numel() * 4 + gp.numel() * 4 + gr.numel() * 4 + r.numel() * 4
+    d2h = dx.numel() * 2 + dw.numel() * 4
+    for _ in range(3):
+        x.copy_(h_x, non_blocking=True)
+        step()
+        h_dx.copy_(dx, non_blocking=True)
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    ea.record(stream)
+    for _ in range(args.e2e_steps):
+        x.copy_(h_x, non_blocking=True)
+        w.copy_(h_w, non_blocking=True)
+        gp.copy_(h_gp, non_blocking=True)
+        gr.copy_(h_gr, non_blocking=True)
+        r.copy_(h_r, non_blocking=True)
+        step()
+        h_dx.copy_(dx, non_blocking=True)
+        h_dw.copy_(dw, non_blocking=True)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * alg / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, toks, secs = _oracle_rate(T, K, seconds=12.0)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": _cpu_threads(), "kind": "oracle",
+               "sample": f"{toks} of {T} tokens x K={K} of the training profile "
+                         f"(512-token slices, {secs:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": mean_ms, "us_per_step": mean_ms * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"training profile T={T} K={K} (4 streams x hidden 5120)",
+                       "T": T, "K": K, "kernel": args.kernel,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                       "algorithmic_bytes_per_step": alg,
+                       "pct_of_hbm_peak": 100.0 * (value / world) / peak,
+                       "wall_s_timed_region": wall},
+            "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": k1_gbs / peak, "traffic": _ncu_traffic(args.kernel),
+                         "kernel": "streaming kernel (dX + dW partials)",
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel_us": k1_ms * 1e3, "reduce_us": k2_ms * 1e3,
+                         "algorithmic_bytes_per_launch": k1_bytes},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    plan.close()
+    return 0
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

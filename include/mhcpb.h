@@ -1,0 +1,161 @@
+/*
+ * mhcpb -- mHC projection/RMS backward for GB300 (sm_103a), C ABI.
+ *
+ * The operation (cuDNN frontend page "DSv4.1 mHC projection/RMS backward",
+ * intro):
+ *
+ *     P  = grad_proj[:, :24]
+ *     dX = P @ W + grad_r / (r * K) * X          (stored BF16)
+ *     dW = P^T @ X                                (stored FP32)
+ *
+ * Both matrix products use operands converted to TF32 (round to nearest,
+ * ties away) with FP32 accumulation; the RMS term is FP32 arithmetic.  dW is
+ * reduced over tokens in a fixed order without atomics, so it is bitwise
+ * reproducible for a given (T, K) on any GB300.  Outputs are overwritten,
+ * never accumulated into.  The last 8 columns of grad_proj are never read.
+ *
+ * The caller-facing shape of the API follows the same page's "Prepared class
+ * API": a plan is created once per shape, reports its scratch size, and each
+ * execute enqueues exactly two kernels on the caller's stream (a streaming
+ * kernel that writes dX and per-chunk dW partials into the workspace, then a
+ * fixed-order reduction of the partials into dW) and allocates nothing.
+ *
+ * Layouts (all compact row-major, the page's "Requirements and tensor
+ * contract"):
+ *     x            BF16 [T, K]
+ *     w            FP32 [24, K]
+ *     grad_proj    FP32 [T, 32]     columns 24..31 ignored, even NaN/Inf
+ *     grad_r, r    FP32 [T]         ([T,1] column vectors); r > 0 required
+ *     dx           BF16 [T, K]      output, overwritten
+ *     dw           FP32 [24, K]     output, overwritten
+ *     grad_x_addend BF16 [T, K]     optional; dX = bf16(fp32(bf16(core)) + fp32(addend)),
+ *                                   the value a separate BF16 add would give
+ *                                   (prime-kernels PR #15, "fused mHC stream gradient")
+ * K counts n_streams * hidden (4 * 5120 = 20480 in the training profile).
+ *
+ * Ownership: the caller owns every buffer and the stream.  The library keeps
+ * no pointer past the return of mhcpb_execute; buffers must stay alive until
+ * the enqueued work completes (and for every replay of a captured graph).
+ * Executions that may overlap on the GPU need their own workspace and outputs.
+ *
+ * Errors: every function returns a status.  On any error nothing is enqueued.
+ * A wait inside a kernel that runs out of time (about one second) ends the
+ * kernel early and records MHCPB_ERR_DEVICE_TIMEOUT in the plan's device
+ * status word, read with mhcpb_get_device_status; the outputs of that
+ * execution are then undefined but the CUDA context stays usable.
+ *
+ * Thread safety: a plan may be used from several host threads; executions on
+ * one plan share its device status word only.
+ */
+#ifndef MHCPB_H
+#define MHCPB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mhcpb_plan_s* mhcpb_plan_t;
+
+typedef enum {
+    MHCPB_OK = 0,
+    MHCPB_ERR_INVALID_ARG = 1,        /* NULL plan/pointer, addend presence disagreeing with the plan */
+    MHCPB_ERR_UNSUPPORTED_SHAPE = 2,  /* T < 1, K not a positive multiple of 8, or above the maxima below */
+    MHCPB_ERR_MISALIGNED = 3,         /* a pointer not 16-byte aligned */
+    MHCPB_ERR_ALIASING = 4,           /* two operands (or workspace) share bytes */
+    MHCPB_ERR_WRONG_DEVICE = 5,       /* a pointer not in device memory of the plan's device */
+    MHCPB_ERR_TF32_NOT_ALLOWED = 6,   /* flags lack MHCPB_ALLOW_TF32 */
+    MHCPB_ERR_WORKSPACE_TOO_SMALL = 7,
+    MHCPB_ERR_CUDA = 8,               /* a CUDA runtime/driver call failed (see mhcpb_last_cuda_error) */
+    MHCPB_ERR_DEVICE_TIMEOUT = 9,     /* reported by mhcpb_get_device_status */
+    MHCPB_ERR_UNSUPPORTED_DEVICE = 10 /* device is not compute capability 10.3 (GB300) */
+} mhcpb_status_t;
+
+/* Plan flags. */
+enum {
+    /* Required: the caller accepts TF32 operands in the matrix products (the
+     * page makes allow_tf32=True mandatory). */
+    MHCPB_ALLOW_TF32 = 1u,
+    /* Executions pass a BF16 grad_x_addend that is added into dX. */
+    MHCPB_HAS_ADDEND = 2u,
+    /* Use the FP32-FMA (CUDA-core) streaming kernel instead of the tensor-core
+     * one.  Same results within tolerance, same determinism; kept as the
+     * measured control for the tensor-core kernel. */
+    MHCPB_FMA_KERNEL = 4u
+};
+
+/* Shape limits (inclusive). */
+#define MHCPB_MAX_T (1 << 24)
+#define MHCPB_MAX_K (1 << 20)
+/* Number of projection columns used, stored width of grad_proj. */
+#define MHCPB_NPROJ 24
+#define MHCPB_GRAD_PROJ_COLS 32
+/* Tokens per dW partial: the token reduction is split into
+ * ceil(T / MHCPB_TOKENS_PER_PARTIAL) fixed chunks, independent of the GPU. */
+#define MHCPB_TOKENS_PER_PARTIAL 512
+
+/* Creates a plan for one shape on one device.  Checks the flags and shape
+ * first (no CUDA call is made when they are rejected), then that `device` is
+ * a compute-capability-10.3 GPU, loads both kernels and allocates the plan's
+ * 4-byte device status word.  `*out` is set only on success. */
+mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int device,
+                                 uint32_t flags);
+
+/* Scratch bytes an execute needs: S * 24 * K * 4 with
+ * S = ceil(T / MHCPB_TOKENS_PER_PARTIAL) (15,728,640 B at T=4096, K=20480).
+ * Contents need no initialisation and are dead after the execute. */
+mhcpb_status_t mhcpb_workspace_bytes(mhcpb_plan_t plan, size_t* bytes);
+
+/* Enqueues the backward on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream).  All pointers are device pointers on the plan's device,
+ * 16-byte aligned and pairwise disjoint; `grad_x_addend` must be NULL unless
+ * the plan has MHCPB_HAS_ADDEND, and non-NULL if it has.  Returns without
+ * synchronising.  Capturable into a CUDA graph (no allocation, no host sync;
+ * tensor maps travel by value in the kernel parameters). */
+mhcpb_status_t mhcpb_execute(mhcpb_plan_t plan,
+                             const void* x, const float* w, const float* grad_proj,
+                             const float* grad_r, const float* r,
+                             void* dx, float* dw,
+                             void* workspace, size_t workspace_bytes,
+                             const void* grad_x_addend, void* stream);
+
+/* mhcpb_execute with timing events for measurement tools: records
+ * `ev_before` (a cudaEvent_t, may be NULL) before the streaming kernel,
+ * `ev_between` after it and `ev_after` after the reduction kernel, all on
+ * `stream`.  The recorded event between the kernels stops the reduction from
+ * starting early, so use plain mhcpb_execute for end-to-end timing. */
+mhcpb_status_t mhcpb_execute_profiled(mhcpb_plan_t plan,
+                                      const void* x, const float* w, const float* grad_proj,
+                                      const float* grad_r, const float* r,
+                                      void* dx, float* dw,
+                                      void* workspace, size_t workspace_bytes,
+                                      const void* grad_x_addend, void* stream,
+                                      void* ev_before, void* ev_between, void* ev_after);
+
+/* Reads (and, if `clear` is nonzero, resets) the plan's device status word.
+ * Synchronises with the device.  *status is MHCPB_OK or the first device-side
+ * error recorded since the last clear (MHCPB_ERR_DEVICE_TIMEOUT). */
+mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status, int clear);
+
+/* Plan facts for tools and tests: which = 0 T, 1 K, 2 partial count S,
+ * 3 grid size of the streaming kernel, 4 flags, 5 streaming-kernel dynamic
+ * shared memory bytes, 6 token tile, 7 column strip width. */
+mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value);
+
+/* Releases the plan (and its status word).  Safe on NULL. */
+mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan);
+
+/* Static description of a status; never NULL. */
+const char* mhcpb_status_string(mhcpb_status_t status);
+
+/* The last CUDA error string seen by this thread inside the library (for
+ * MHCPB_ERR_CUDA), or "" if none. */
+const char* mhcpb_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHCPB_H */

@@ -265,3 +265,28 @@ def check_dw(dw, ref_f64, abs_bound, rel=1e-3):
     with np.errstate(divide="ignore", invalid="ignore"):
         worst = float(np.max(np.where(lim > 0, diff / lim, np.where(diff > 0, np.inf, 0.0)))) if dw.size else 0.0
     return bool(ok.all()), dict(n=int(dw.size), fail=int((~ok).sum()), worst_frac_of_tol=worst)
+
+
+def check_dx_addend(dx_bits, ref_bits, core_ref_bits, core_abs_bound, ulps=2.0,
+                    rel_abs=2.0 ** -16):
+    """dX acceptance with the fused addend.
+
+    The addend is added after the core is rounded to BF16, so a core that is
+    within tolerance of the oracle's core (``ulps`` BF16 places, or the FP32
+    accumulation bound under cancellation) moves the sum by at most that much
+    plus one rounding of the sum.  An element passes when |dx - ref| is within
+    ``ulps`` places of the reference sum, or within
+    ulps * ulp(core_ref) + rel_abs * core_abs_bound + ulp(ref).
+    """
+    a = bf16_bits_to_f64(dx_bits)
+    b = bf16_bits_to_f64(ref_bits)
+    core = bf16_bits_to_f64(core_ref_bits)
+    fin = np.isfinite(b)
+    diff = np.abs(np.where(fin, a - b, 0.0))
+    u = bf16_ulp(b)
+    lim = np.maximum(ulps * u, ulps * bf16_ulp(core) + rel_abs * np.asarray(core_abs_bound) + u)
+    ok_elem = np.where(fin, (diff <= lim) & np.isfinite(a), (np.isnan(a) & np.isnan(b)) | (a == b))
+    stats = dict(n=int(a.size), fail=int((~ok_elem).sum()),
+                 exact=int((np.asarray(dx_bits) == np.asarray(ref_bits)).sum()),
+                 max_ulp=float(np.max(np.where(fin, diff / u, 0.0))) if a.size else 0.0)
+    return bool(ok_elem.all()), stats

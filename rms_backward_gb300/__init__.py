@@ -1,1 +1,90 @@
-"""GB300-native mHC projection/RMS backward (sm_103a CUDA kernels behind a C-ABI)."""
+"""GB300-native mHC projection/RMS backward.
+
+    P  = grad_proj[:, :24]
+    dX = P @ W + grad_r / (r * K) * X        (BF16)
+    dW = P.T @ X                              (FP32, fixed-order reduction)
+
+The computation runs in two sm_103a CUDA kernels behind the C ABI of
+``include/mhcpb.h`` (``libmhcpb.so``).  This package is the Python side:
+``abi`` binds the C functions by name; :class:`Plan` and
+:func:`mhc_projection_backward` marshal torch CUDA tensors into them (torch
+supplies device memory and streams only).
+"""
+from __future__ import annotations
+
+from . import abi
+from .abi import (  # noqa: F401
+    MHCPB_ALLOW_TF32, MHCPB_FMA_KERNEL, MHCPB_HAS_ADDEND, MhcpbError, mhcpb_destroy,
+    mhcpb_execute, mhcpb_get_device_status, mhcpb_last_cuda_error, mhcpb_plan_create,
+    mhcpb_plan_query, mhcpb_status_string, mhcpb_workspace_bytes,
+)
+
+
+class Plan:
+    """A prepared backward for one (T, K) on one device (owns a C plan handle)."""
+
+    def __init__(self, T: int, K: int, device: int = 0, *, addend: bool = False,
+                 fma_kernel: bool = False):
+        flags = abi.MHCPB_ALLOW_TF32
+        if addend:
+            flags |= abi.MHCPB_HAS_ADDEND
+        if fma_kernel:
+            flags |= abi.MHCPB_FMA_KERNEL
+        self.T, self.K, self.device, self.flags = int(T), int(K), int(device), flags
+        self.handle = mhcpb_plan_create(T, K, device, flags)
+        self.workspace_bytes = mhcpb_workspace_bytes(self.handle)
+
+    def query(self, which: str) -> int:
+        return mhcpb_plan_query(self.handle, which)
+
+    def execute(self, x, w, grad_proj, grad_r, r, dx, dw, workspace, addend=None, stream=None):
+        """Enqueue on ``stream`` (a torch.cuda.Stream, a raw handle, or None for
+        the current stream of the tensors' device)."""
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream(x.device).cuda_stream
+        elif hasattr(stream, "cuda_stream"):
+            stream = stream.cuda_stream
+        mhcpb_execute(self.handle, x.data_ptr(), w.data_ptr(), grad_proj.data_ptr(),
+                      grad_r.data_ptr(), r.data_ptr(), dx.data_ptr(), dw.data_ptr(),
+                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                      None if addend is None else addend.data_ptr(), stream)
+
+    def device_status(self, clear: bool = False) -> int:
+        return mhcpb_get_device_status(self.handle, clear)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            mhcpb_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def mhc_projection_backward(x, weight, grad_proj, grad_r, r, addend=None, *, stream=None,
+                            fma_kernel: bool = False):
+    """Allocating convenience call: returns (dx BF16 [T,K], dw FP32 [24,K]).
+
+    Outputs and workspace are allocated by torch on the tensors' device.  The
+    call waits for the stream before it returns (it owns a temporary plan).
+    """
+    import torch
+    T, K = x.shape
+    plan = Plan(T, K, x.device.index or 0, addend=addend is not None, fma_kernel=fma_kernel)
+    dx = torch.empty((T, K), dtype=torch.bfloat16, device=x.device)
+    dw = torch.empty((24, K), dtype=torch.float32, device=x.device)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=x.device)
+    plan.execute(x, weight, grad_proj, grad_r, r, dx, dw, ws, addend=addend, stream=stream)
+    # the plan (its status word) and the workspace must outlive the enqueued work
+    if stream is None:
+        torch.cuda.current_stream(x.device).synchronize()
+    elif hasattr(stream, "synchronize"):
+        stream.synchronize()
+    else:
+        torch.cuda.synchronize(x.device)
+    plan.close()
+    return dx, dw

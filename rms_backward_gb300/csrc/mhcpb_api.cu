@@ -1,0 +1,333 @@
+// Host side of the C ABI declared in include/mhcpb.h: plan creation, the
+// tensor contract checks of the cuDNN frontend page "DSv4.1 mHC
+// projection/RMS backward" ("Requirements and tensor contract"), TMA tensor
+// map encoding and the two launches of one execute ("Prepared class API":
+// execute enqueues exactly two kernels and allocates nothing).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "mhcpb.h"
+#include "mhcpb_internal.h"
+
+using namespace mhcpb;
+
+struct mhcpb_plan_s {
+    int64_t T = 0, K = 0;
+    int device = 0;
+    uint32_t flags = 0;
+    int S = 0;            // dW partials
+    int n_strips = 0;     // strips of the streaming kernel in use
+    int grid = 0;         // CTAs of the streaming kernel
+    size_t ws_bytes = 0;
+    size_t smem = 0;
+    uint32_t* d_status = nullptr;
+    uint64_t timeout_ns = 1000000000ull;  // 1 s bound on every in-kernel wait
+};
+
+namespace {
+
+thread_local char g_cuda_err[256] = "";
+
+mhcpb_status_t cuda_fail(cudaError_t e, const char* what) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", what, cudaGetErrorString(e));
+    return MHCPB_ERR_CUDA;
+}
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn get_encode() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+// BF16 [T, K] row-major tensor, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool encode_bf16_map(CUtensorMap* m, const void* base, int64_t T, int64_t K, uint32_t box_rows) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)tc::kBoxCols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Range {
+    uintptr_t lo, hi;
+};
+bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+mhcpb_status_t check_device_ptr(const void* ptr, int device) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return MHCPB_ERR_WRONG_DEVICE;
+    }
+    if ((a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) || a.device != device)
+        return MHCPB_ERR_WRONG_DEVICE;
+    return MHCPB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mhcpb_status_string(mhcpb_status_t s) {
+    switch (s) {
+        case MHCPB_OK: return "ok";
+        case MHCPB_ERR_INVALID_ARG: return "invalid argument";
+        case MHCPB_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (T >= 1, K a positive multiple of 8, within limits)";
+        case MHCPB_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case MHCPB_ERR_ALIASING: return "operands overlap";
+        case MHCPB_ERR_WRONG_DEVICE: return "pointer not in device memory of the plan's device";
+        case MHCPB_ERR_TF32_NOT_ALLOWED: return "MHCPB_ALLOW_TF32 is required";
+        case MHCPB_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MHCPB_ERR_CUDA: return "CUDA error";
+        case MHCPB_ERR_DEVICE_TIMEOUT: return "a wait inside the kernel timed out";
+        case MHCPB_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3";
+    }
+    return "unknown status";
+}
+
+const char* mhcpb_last_cuda_error(void) { return g_cuda_err; }
+
+mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int device,
+                                 uint32_t flags) {
+    if (out == nullptr) return MHCPB_ERR_INVALID_ARG;
+    if ((flags & MHCPB_ALLOW_TF32) == 0) return MHCPB_ERR_TF32_NOT_ALLOWED;
+    if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND | MHCPB_FMA_KERNEL)) != 0)
+        return MHCPB_ERR_INVALID_ARG;
+    if (T < 1 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
+        return MHCPB_ERR_UNSUPPORTED_SHAPE;
+    if (device < 0) return MHCPB_ERR_INVALID_ARG;
+
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+    if (device >= ndev) return MHCPB_ERR_INVALID_ARG;
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3) return MHCPB_ERR_UNSUPPORTED_DEVICE;
+
+    DeviceGuard g(device);
+    if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
+
+    const bool fma_kernel = (flags & MHCPB_FMA_KERNEL) != 0;
+    const bool add = (flags & MHCPB_HAS_ADDEND) != 0;
+    if (fma_kernel) {
+        if ((e = fma::setup()) != cudaSuccess) return cuda_fail(e, "setup (FMA kernel)");
+    } else {
+        if (!get_encode()) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
+        if ((e = tc::setup(add)) != cudaSuccess) return cuda_fail(e, "setup (tensor-core kernel)");
+    }
+
+    mhcpb_plan_s* p = new mhcpb_plan_s();
+    p->T = T;
+    p->K = K;
+    p->device = device;
+    p->flags = flags;
+    p->S = (int)((T + kTokensPerPartial - 1) / kTokensPerPartial);
+    p->ws_bytes = (size_t)p->S * kNProj * (size_t)K * sizeof(float);
+    if (fma_kernel) {
+        p->n_strips = (int)((K + fma::kStrip - 1) / fma::kStrip);
+        p->grid = p->n_strips * p->S;
+        p->smem = fma::smem_bytes();
+    } else {
+        p->n_strips = (int)((K + tc::kStrip - 1) / tc::kStrip);
+        const int64_t items = (int64_t)p->n_strips * p->S;
+        p->grid = (int)(items < sms ? items : sms);
+        p->smem = tc::smem_bytes(add);
+    }
+    if ((e = cudaMalloc(&p->d_status, sizeof(uint32_t))) != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "cudaMalloc (status word)");
+    }
+    if ((e = cudaMemset(p->d_status, 0, sizeof(uint32_t))) != cudaSuccess) {
+        cudaFree(p->d_status);
+        delete p;
+        return cuda_fail(e, "cudaMemset (status word)");
+    }
+    *out = p;
+    return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_workspace_bytes(mhcpb_plan_t plan, size_t* bytes) {
+    if (plan == nullptr || bytes == nullptr) return MHCPB_ERR_INVALID_ARG;
+    *bytes = plan->ws_bytes;
+    return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value) {
+    if (plan == nullptr || value == nullptr) return MHCPB_ERR_INVALID_ARG;
+    switch (which) {
+        case 0: *value = plan->T; break;
+        case 1: *value = plan->K; break;
+        case 2: *value = plan->S; break;
+        case 3: *value = plan->grid; break;
+        case 4: *value = plan->flags; break;
+        case 5: *value = (int64_t)plan->smem; break;
+        case 6: *value = (plan->flags & MHCPB_FMA_KERNEL) ? kTokensPerPartial : tc::kTokenTile; break;
+        case 7: *value = (plan->flags & MHCPB_FMA_KERNEL) ? fma::kStrip : tc::kStrip; break;
+        default: return MHCPB_ERR_INVALID_ARG;
+    }
+    return MHCPB_OK;
+}
+
+static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float* w,
+                                   const float* grad_proj, const float* grad_r, const float* r,
+                                   void* dx, float* dw, void* workspace, size_t workspace_bytes,
+                                   const void* grad_x_addend, void* stream, void* ev0, void* ev1,
+                                   void* ev2) {
+    if (plan == nullptr) return MHCPB_ERR_INVALID_ARG;
+    const bool add = (plan->flags & MHCPB_HAS_ADDEND) != 0;
+    if (!x || !w || !grad_proj || !grad_r || !r || !dx || !dw || !workspace)
+        return MHCPB_ERR_INVALID_ARG;
+    if (add != (grad_x_addend != nullptr)) return MHCPB_ERR_INVALID_ARG;
+    if (workspace_bytes < plan->ws_bytes) return MHCPB_ERR_WORKSPACE_TOO_SMALL;
+
+    const int64_t T = plan->T, K = plan->K;
+    const void* ptrs[9] = {x, w, grad_proj, grad_r, r, dx, dw, workspace, grad_x_addend};
+    const size_t sizes[9] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4), (size_t)(T * kGradProjCols * 4),
+                             (size_t)(T * 4), (size_t)(T * 4), (size_t)(T * K * 2),
+                             (size_t)(kNProj * K * 4), plan->ws_bytes, (size_t)(T * K * 2)};
+    const int n = add ? 9 : 8;
+    for (int i = 0; i < n; ++i)
+        if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != 0) return MHCPB_ERR_MISALIGNED;
+    Range rg[9];
+    for (int i = 0; i < n; ++i) {
+        rg[i].lo = reinterpret_cast<uintptr_t>(ptrs[i]);
+        rg[i].hi = rg[i].lo + sizes[i];
+    }
+    for (int i = 0; i < n; ++i)
+        for (int j = i + 1; j < n; ++j)
+            if (overlap(rg[i], rg[j])) return MHCPB_ERR_ALIASING;
+    for (int i = 0; i < n; ++i) {
+        mhcpb_status_t s = check_device_ptr(ptrs[i], plan->device);
+        if (s != MHCPB_OK) return s;
+    }
+
+    DeviceGuard g(plan->device);
+    if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    MainParams p{};
+    p.T = (int32_t)T;
+    p.K = (int32_t)K;
+    p.S = plan->S;
+    p.n_strips = plan->n_strips;
+    p.x = static_cast<const uint16_t*>(x);
+    p.w = w;
+    p.grad_proj = grad_proj;
+    p.grad_r = grad_r;
+    p.r = r;
+    p.dx = static_cast<uint16_t*>(dx);
+    p.addend = static_cast<const uint16_t*>(grad_x_addend);
+    p.partial = static_cast<float*>(workspace);
+    p.status = plan->d_status;
+    p.timeout_ns = plan->timeout_ns;
+
+    cudaError_t e;
+    if (ev0 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev0), st)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord");
+    if (plan->flags & MHCPB_FMA_KERNEL) {
+        e = fma::launch(p, st);
+        if (e != cudaSuccess) return cuda_fail(e, "launch (FMA kernel)");
+    } else {
+        CUtensorMap xm, dxm, am;
+        if (!encode_bf16_map(&xm, x, T, K, tc::kTokenTile) || !encode_bf16_map(&dxm, dx, T, K, 32) ||
+            !encode_bf16_map(&am, add ? grad_x_addend : x, T, K, tc::kTokenTile))
+            return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+        e = tc::launch(p, xm, dxm, am, plan->grid, st);
+        if (e != cudaSuccess) return cuda_fail(e, "launch (tensor-core kernel)");
+    }
+    if (ev1 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev1), st)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord");
+    e = launch_reduce(p.partial, dw, plan->S, (int64_t)kNProj * K, st);
+    if (e != cudaSuccess) return cuda_fail(e, "launch (dW reduction)");
+    if (ev2 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev2), st)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord");
+    return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_execute(mhcpb_plan_t plan, const void* x, const float* w,
+                             const float* grad_proj, const float* grad_r, const float* r, void* dx,
+                             float* dw, void* workspace, size_t workspace_bytes,
+                             const void* grad_x_addend, void* stream) {
+    return execute_impl(plan, x, w, grad_proj, grad_r, r, dx, dw, workspace, workspace_bytes,
+                        grad_x_addend, stream, nullptr, nullptr, nullptr);
+}
+
+mhcpb_status_t mhcpb_execute_profiled(mhcpb_plan_t plan, const void* x, const float* w,
+                                      const float* grad_proj, const float* grad_r, const float* r,
+                                      void* dx, float* dw, void* workspace, size_t workspace_bytes,
+                                      const void* grad_x_addend, void* stream, void* ev_before,
+                                      void* ev_between, void* ev_after) {
+    return execute_impl(plan, x, w, grad_proj, grad_r, r, dx, dw, workspace, workspace_bytes,
+                        grad_x_addend, stream, ev_before, ev_between, ev_after);
+}
+
+mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status, int clear) {
+    if (plan == nullptr || status == nullptr) return MHCPB_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpy(&v, plan->d_status, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy (status word)");
+    if (clear && v != 0) {
+        e = cudaMemset(plan->d_status, 0, sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset (status word)");
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    }
+    *status = static_cast<mhcpb_status_t>(v);
+    return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan) {
+    if (plan == nullptr) return MHCPB_OK;
+    if (plan->d_status) {
+        DeviceGuard g(plan->device);
+        cudaFree(plan->d_status);
+    }
+    delete plan;
+    return MHCPB_OK;
+}
+
+}  // extern "C"

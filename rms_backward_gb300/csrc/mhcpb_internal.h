@@ -1,0 +1,59 @@
+// Internal interface between the C-ABI host code and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mhcpb {
+
+constexpr int kNProj = 24;          // projection columns used (P = grad_proj[:, :24])
+constexpr int kGradProjCols = 32;   // stored width of grad_proj
+constexpr int kTokensPerPartial = 512;  // tokens per dW partial (fixed chunk)
+
+// Device status word values (match mhcpb_status_t).
+constexpr uint32_t kDevOk = 0;
+constexpr uint32_t kDevTimeout = 9;
+
+// Everything the streaming kernels need besides the tensor maps.
+struct MainParams {
+    int32_t T;
+    int32_t K;
+    int32_t S;            // number of dW partials = ceil(T / kTokensPerPartial)
+    int32_t n_strips;     // ceil(K / strip width) of the kernel in use
+    const uint16_t* x;    // BF16 [T, K] (FMA kernel reads it directly)
+    const float* w;       // [24, K]
+    const float* grad_proj;  // [T, 32]
+    const float* grad_r;  // [T]
+    const float* r;       // [T]
+    uint16_t* dx;         // BF16 [T, K] (FMA kernel writes it directly)
+    const uint16_t* addend;  // BF16 [T, K] or null
+    float* partial;       // [S, 24, K]
+    uint32_t* status;     // device status word
+    uint64_t timeout_ns;  // bound on every wait inside the kernel
+};
+
+// Tensor-core (tcgen05 + TMA) streaming kernel: geometry and launch.
+namespace tc {
+constexpr int kTokenTile = 128;    // MMA M for dX; K-extent of one dW MMA group
+constexpr int kStrip = 128;        // columns per strip: MMA N for dX, M for dW
+constexpr int kBoxCols = 64;       // TMA box width (128 bytes of BF16)
+constexpr int kThreads = 256;
+size_t smem_bytes(bool has_addend);
+cudaError_t setup(bool has_addend);
+cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensorMap& dx_map,
+                   const CUtensorMap& add_map, int grid, cudaStream_t stream);
+}  // namespace tc
+
+// FP32-FMA (CUDA core) streaming kernel: the measured control.
+namespace fma {
+constexpr int kStrip = 64;
+constexpr int kThreads = 256;
+size_t smem_bytes();
+cudaError_t setup();
+cudaError_t launch(const MainParams& p, cudaStream_t stream);
+}  // namespace fma
+
+// Second kernel: dW[j,k] = sum over s ascending of partial[s][j][k].
+cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, cudaStream_t stream);
+
+}  // namespace mhcpb

@@ -1,0 +1,561 @@
+// Tensor-core streaming kernel of the mHC projection/RMS backward (sm_103a).
+//
+// What it computes (cuDNN frontend page "DSv4.1 mHC projection/RMS backward",
+// intro): for every token t and column k,
+//   dX[t,k]          = sum_j P[t,j] W[j,k] + c[t] X[t,k],   c = grad_r / (r K)
+//   partial[s][j][k] = sum_{t in chunk s} P[t,j] X[t,k]      (chunk = 512 tokens)
+// with P = grad_proj[:, :24] and W rounded to TF32 (nearest, ties away) and
+// FP32 accumulation.  The second kernel sums the partials in a fixed order.
+//
+// How, on GB300:
+//  * The grid is persistent (one CTA per SM).  Work items are (128-column
+//    strip, 512-token chunk) pairs in strip-major order; a CTA takes a
+//    contiguous range of them, so W for a strip is staged once per strip.
+//    The chunking depends only on T, so dW bits do not depend on the SM count.
+//  * X arrives by TMA in 128-token x 128-column tiles (two 64-column boxes,
+//    128-byte swizzle) into a ring of shared-memory stages; X is read from
+//    HBM exactly once.
+//  * Both contractions run on the tensor cores (tcgen05.mma kind::f16, BF16
+//    operands, FP32 accumulators in TMEM).  A TF32 value has 11 significant
+//    bits, so it is exactly hi + lo with hi, lo BF16 (hi = bf16(v),
+//    lo = v - hi).  With P = Ph + Pl and W = Wh + Wl, every product the MMA
+//    forms is exact, exactly as a TF32 product would be:
+//        dX tile  = [Ph Pl] x [Wh; Wh] + [Ph Pl] x [Wl; Wl]      (M128 N128 K96)
+//        dW^T     = X^T x [Ph Pl]   (X used in place, MN-major; M128 N48 K128)
+//    X itself is BF16, a subset of TF32, and needs no conversion.
+//  * Four epilogue warps read the dX accumulator from TMEM, add c*X (FP32 FMA,
+//    X from the same shared-memory tile), round to BF16 (and add the optional
+//    BF16 addend the way a separate BF16 add would), write the result over
+//    the X tile in place and TMA-store it.  At the end of each chunk they
+//    write the chunk's dW partial (hi and lo halves summed) to the workspace.
+//  * Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2 operand
+//    preparation (TF32 rounding and BF16 hi/lo split of P and W into the
+//    tensor-core operand layout), 4-7 epilogue.
+//  * Every mbarrier wait is bounded (see wait_bar): on timeout the kernel
+//    records a status word, drains its own copies and MMAs and exits.
+#include <cuda_bf16.h>
+
+#include "mhcpb_internal.h"
+#include "ptx.cuh"
+
+namespace mhcpb {
+namespace tc {
+
+namespace {
+
+constexpr int kChunk = kTokensPerPartial;
+constexpr int kNJS = 2 * kNProj;                         // 48 split P columns
+constexpr uint32_t kXTile = kTokenTile * kStrip * 2;     // 32 KiB of BF16
+constexpr uint32_t kBoxBytes = kTokenTile * kBoxCols * 2;  // 16 KiB (one 64-column box)
+constexpr uint32_t kPStage = kTokenTile * kNJS * 2;      // 12 KiB
+constexpr uint32_t kWBytes = kStrip * 64 * 2;            // 16 KiB (8 blocks of 8 per column group)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDwCol = 256;                         // dW accumulators at 256 and 320
+constexpr uint32_t kDwColStride = 64;
+
+template <bool ADD>
+struct Cfg {
+    static constexpr int NS = ADD ? 3 : 5;               // X (+addend) stages
+    static constexpr int NP = ADD ? 1 : 2;               // split-P stages
+    static constexpr uint32_t stage_bytes = ADD ? 2 * kXTile : kXTile;
+    static constexpr uint32_t off_p = NS * stage_bytes;
+    static constexpr uint32_t off_w = off_p + NP * kPStage;
+    static constexpr uint32_t off_bar = off_w + kWBytes;
+    // barriers: x_full[NS] x_empty[NS] p_full[NP] p_empty[NP] acc_full[2]
+    //           acc_empty[2] dw_full[2] dw_empty[2] w_full w_empty fin
+    static constexpr int B_XF = 0, B_XE = NS, B_PF = 2 * NS, B_PE = 2 * NS + NP;
+    static constexpr int B_AF = 2 * NS + 2 * NP, B_AE = B_AF + 2, B_DF = B_AF + 4,
+                         B_DE = B_AF + 6, B_WF = B_AF + 8, B_WE = B_AF + 9, B_FIN = B_AF + 10;
+    static constexpr int n_bars = B_FIN + 1;
+    static constexpr uint32_t off_misc = off_bar + n_bars * 8;
+    static constexpr uint32_t bytes = off_misc + 16;
+    static constexpr uint32_t alloc = bytes + 1024;      // room to align the base to 1 KiB
+};
+
+// Bounded mbarrier wait.  Returns false when the CTA is aborting (another role
+// timed out) or when this wait exceeded the time limit; in the latter case it
+// raises the CTA's abort flag and records the timeout in the status word.
+// With honor_abort == false it keeps waiting (still bounded) while aborting:
+// used to drain a role's own in-flight copies and MMAs before exit.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                      uint32_t* status, uint64_t timeout_ns, bool honor_abort) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0) {
+            if (honor_abort && *abort_flag) return false;
+            if (ptx::globaltimer() - t0 > timeout_ns) {
+                *abort_flag = 1u;
+                atomicCAS(status, kDevOk, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float tf32_rna(float v) {
+    uint32_t u;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(v));
+    return __uint_as_float(u & 0xFFFFE000u);
+}
+
+// TF32 value -> (hi, lo) BF16 with hi + lo == v exactly (v finite).  A
+// non-finite v keeps lo = 0 so that Inf stays Inf instead of Inf - Inf.
+__device__ __forceinline__ void split_tf32(float v, uint16_t& hi, uint16_t& lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    const float rem = isfinite(v) ? v - __bfloat162float(h) : 0.f;
+    const __nv_bfloat16 l = __float2bfloat16_rn(rem);
+    hi = *reinterpret_cast<const uint16_t*>(&h);
+    lo = *reinterpret_cast<const uint16_t*>(&l);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Work-item geometry shared by all roles.
+struct Item {
+    int strip, chunk, col0, t_begin, ntiles;
+};
+__device__ __forceinline__ Item item_at(const MainParams& p, int it) {
+    Item r;
+    r.strip = it / p.S;
+    r.chunk = it - r.strip * p.S;
+    r.col0 = r.strip * kStrip;
+    r.t_begin = r.chunk * kChunk;
+    const int t_end = min(p.T, r.t_begin + kChunk);
+    r.ntiles = (t_end - r.t_begin + kTokenTile - 1) / kTokenTile;
+    return r;
+}
+
+// Shared-memory operand layouts written by the preparation warp (no swizzle,
+// 8-row x 16-byte core matrices of 128 contiguous bytes):
+//  P split  [token/8][jb 0..5][token%8][8 BF16]: jb 0,1 = Ph[0..15], 2,3 = Pl[0..15],
+//           4 = Ph[16..23], 5 = Pl[16..23].  Read as the K-major A operand of the
+//           dX MMA (M = token, K = split column) and as the MN-major B operand of
+//           the dW MMA (N = split column, K = token).
+//  W split  [col/8][wb 0..7][col%8][8 BF16]: wb 0,1 = Wh[0..15], 2 = 3 = Wh[16..23],
+//           4,5 = Wl[0..15], 6 = 7 = Wl[16..23].  K-major B operand of the dX MMA.
+// dX k-steps (16 split columns each) pair A blocks {0,2,4,0,2,4} with W blocks
+// {0,0,2,4,4,6}: Ph.Wh + Pl.Wh + [Ph Pl]16..23.[Wh Wh] + the same with Wl.
+__device__ __forceinline__ uint32_t p_off(int tok, int jb) {
+    return (uint32_t)(((tok >> 3) * 6 + jb) * 128 + (tok & 7) * 16);
+}
+__device__ __forceinline__ uint32_t w_off(int col, int wb) {
+    return (uint32_t)(((col >> 3) * 8 + wb) * 128 + (col & 7) * 16);
+}
+
+template <bool ADD>
+__global__ void __launch_bounds__(kThreads, 1)
+    main_tc_kernel(const MainParams p, const __grid_constant__ CUtensorMap x_map,
+                   const __grid_constant__ CUtensorMap dx_map,
+                   const __grid_constant__ CUtensorMap add_map) {
+    using C = Cfg<ADD>;
+    constexpr int NS = C::NS, NP = C::NP;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::off_misc);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::off_misc + 4);
+    auto bar = [&](int i) -> uint32_t { return sbase + C::off_bar + 8u * (uint32_t)i; };
+
+    const int n_items = p.n_strips * p.S;
+    const int it_begin = (int)((int64_t)blockIdx.x * n_items / gridDim.x);
+    const int it_end = (int)((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(bar(C::B_XF + s), 1);
+            ptx::mbar_init(bar(C::B_XE + s), 4);
+        }
+        for (int s = 0; s < NP; ++s) {
+            ptx::mbar_init(bar(C::B_PF + s), 1);
+            ptx::mbar_init(bar(C::B_PE + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(C::B_AF + b), 1);
+            ptx::mbar_init(bar(C::B_AE + b), 4);
+            ptx::mbar_init(bar(C::B_DF + b), 1);
+            ptx::mbar_init(bar(C::B_DE + b), 4);
+        }
+        ptx::mbar_init(bar(C::B_WF), 1);
+        ptx::mbar_init(bar(C::B_WE), 1);
+        ptx::mbar_init(bar(C::B_FIN), 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&x_map);
+        ptx::prefetch_tensormap(&dx_map);
+        if (ADD) ptx::prefetch_tensormap(&add_map);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    ptx::grid_launch_dependents();
+
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol = ptx::policy_evict_first();
+            int st = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0, last_par = 0;
+            bool ok = true;
+            for (int it = it_begin; it < it_end && ok; ++it) {
+                const Item I = item_at(p, it);
+                for (int tt = 0; tt < I.ntiles; ++tt) {
+                    if (!wait_bar(bar(C::B_XE + st), ph ^ 1u, abort_flag, p.status, tmo, true)) {
+                        ok = false;
+                        break;
+                    }
+                    const int tok0 = I.t_begin + tt * kTokenTile;
+                    const uint32_t dst = sbase + (uint32_t)st * C::stage_bytes;
+                    ptx::mbar_arrive_expect_tx(bar(C::B_XF + st), C::stage_bytes);
+                    ptx::tma_load_2d(dst, &x_map, I.col0, tok0, bar(C::B_XF + st), pol);
+                    ptx::tma_load_2d(dst + kBoxBytes, &x_map, I.col0 + kBoxCols, tok0,
+                                     bar(C::B_XF + st), pol);
+                    if (ADD) {
+                        ptx::tma_load_2d(dst + kXTile, &add_map, I.col0, tok0, bar(C::B_XF + st),
+                                         pol);
+                        ptx::tma_load_2d(dst + kXTile + kBoxBytes, &add_map, I.col0 + kBoxCols,
+                                         tok0, bar(C::B_XF + st), pol);
+                    }
+                    issued |= 1u << st;
+                    last_par = (last_par & ~(1u << st)) | (ph << st);
+                    if (++st == NS) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // drain: every load this thread issued has landed before the CTA exits
+            for (int s = 0; s < NS; ++s)
+                if (issued & (1u << s))
+                    wait_bar(bar(C::B_XF + s), (last_par >> s) & 1u, abort_flag, p.status, tmo,
+                             false);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_dx = ptx::idesc_bf16_f32(128, kStrip, false, false);
+            constexpr uint32_t idesc_dw = ptx::idesc_bf16_f32(128, kNJS, true, true);
+            const uint32_t a_blk[6] = {0, 2, 4, 0, 2, 4};
+            const uint32_t b_blk[6] = {0, 0, 2, 4, 4, 6};
+            const uint32_t w_base = sbase + C::off_w;
+            int xs = 0, ps = 0, ab = 0;
+            uint32_t xph = 0, pph = 0, aph = 0;
+            int n_w = 0, prev_strip = -1, local = 0;
+            bool ok = true;
+            for (int it = it_begin; it < it_end && ok; ++it, ++local) {
+                const Item I = item_at(p, it);
+                const int db = local & 1;
+                const uint32_t dph = (uint32_t)(local >> 1) & 1u;
+                if (I.strip != prev_strip) {
+                    if (!wait_bar(bar(C::B_WF), (uint32_t)n_w & 1u, abort_flag, p.status, tmo,
+                                  true)) {
+                        ok = false;
+                        break;
+                    }
+                    ++n_w;
+                }
+                if (!wait_bar(bar(C::B_DE + db), dph ^ 1u, abort_flag, p.status, tmo, true)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t d_dw = tmem + kDwCol + (uint32_t)db * kDwColStride;
+                for (int tt = 0; tt < I.ntiles; ++tt) {
+                    if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true) ||
+                        !wait_bar(bar(C::B_PF + ps), pph, abort_flag, p.status, tmo, true) ||
+                        !wait_bar(bar(C::B_AE + ab), aph ^ 1u, abort_flag, p.status, tmo, true)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t pA = sbase + C::off_p + (uint32_t)ps * kPStage;
+                    const uint32_t xA = sbase + (uint32_t)xs * C::stage_bytes;
+                    const uint32_t d_dx = tmem + (uint32_t)ab * kStrip;
+                    // dX = [Ph Pl](x)[Wh;Wh] + [Ph Pl](x)[Wl;Wl]: M=128 tokens, N=128 cols
+#pragma unroll
+                    for (int k = 0; k < 6; ++k) {
+                        const uint64_t da = ptx::smem_desc(pA + a_blk[k] * 128u, 128u, 768u,
+                                                           ptx::kLayoutInterleave);
+                        const uint64_t dbd = ptx::smem_desc(w_base + b_blk[k] * 128u, 128u, 1024u,
+                                                            ptx::kLayoutInterleave);
+                        ptx::mma_bf16(d_dx, da, dbd, idesc_dx, k > 0 ? 1u : 0u);
+                    }
+                    // dW^T += X^T [Ph Pl]: M=128 cols, N=48, K=128 tokens in 8 steps
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint64_t da = ptx::smem_desc(xA + (uint32_t)k * 2048u, kBoxBytes,
+                                                           1024u, ptx::kLayoutSwizzle128B);
+                        const uint64_t dbd = ptx::smem_desc(pA + (uint32_t)k * 1536u, 768u, 128u,
+                                                            ptx::kLayoutInterleave);
+                        ptx::mma_bf16(d_dw, da, dbd, idesc_dw, (tt > 0 || k > 0) ? 1u : 0u);
+                    }
+                    ptx::tc_commit(bar(C::B_PE + ps));
+                    ptx::tc_commit(bar(C::B_AF + ab));
+                    if (++xs == NS) { xs = 0; xph ^= 1u; }
+                    if (++ps == NP) { ps = 0; pph ^= 1u; }
+                    if (++ab == 2) { ab = 0; aph ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::tc_commit(bar(C::B_DF + db));
+                const int next_strip = (it + 1 < it_end) ? (it + 1) / p.S : -1;
+                if (next_strip != I.strip) ptx::tc_commit(bar(C::B_WE));
+                prev_strip = I.strip;
+            }
+            // drain: all MMAs issued by this thread complete before TMEM/smem go away
+            ptx::tc_commit(bar(C::B_FIN));
+            wait_bar(bar(C::B_FIN), 0u, abort_flag, p.status, tmo, false);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ operand preparation
+        int ps = 0;
+        uint32_t pph = 0;
+        int n_w = 0, prev_strip = -1;
+        bool ok = true;
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const Item I = item_at(p, it);
+            if (I.strip != prev_strip) {
+                if (n_w > 0 && !wait_bar(bar(C::B_WE), (uint32_t)(n_w - 1) & 1u, abort_flag,
+                                         p.status, tmo, true)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* wsm = smem + C::off_w;
+                for (int cc = lane; cc < kStrip; cc += 32) {
+                    const int col = I.col0 + cc;
+                    uint16_t hi[kNProj], lo[kNProj];
+#pragma unroll
+                    for (int j = 0; j < kNProj; ++j) {
+                        const float v = col < p.K ? tf32_rna(__ldg(p.w + (size_t)j * p.K + col)) : 0.f;
+                        split_tf32(v, hi[j], lo[j]);
+                    }
+                    const uint16_t* src[8] = {hi, hi + 8, hi + 16, hi + 16, lo, lo + 8, lo + 16, lo + 16};
+#pragma unroll
+                    for (int wb = 0; wb < 8; ++wb) {
+                        uint4 v;
+                        v.x = src[wb][0] | ((uint32_t)src[wb][1] << 16);
+                        v.y = src[wb][2] | ((uint32_t)src[wb][3] << 16);
+                        v.z = src[wb][4] | ((uint32_t)src[wb][5] << 16);
+                        v.w = src[wb][6] | ((uint32_t)src[wb][7] << 16);
+                        *reinterpret_cast<uint4*>(wsm + w_off(cc, wb)) = v;
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(C::B_WF));
+                ++n_w;
+                prev_strip = I.strip;
+            }
+            for (int tt = 0; tt < I.ntiles; ++tt) {
+                const int tok0 = I.t_begin + tt * kTokenTile;
+                // fetch this lane's four P rows before waiting for the stage
+                float4 pr[4][6];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = tok0 + lane + 32 * i;
+                    const float4* g = reinterpret_cast<const float4*>(p.grad_proj + (size_t)row * kGradProjCols);
+#pragma unroll
+                    for (int q = 0; q < 6; ++q)
+                        pr[i][q] = row < p.T ? __ldg(g + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                if (!wait_bar(bar(C::B_PE + ps), pph ^ 1u, abort_flag, p.status, tmo, true)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* psm = smem + C::off_p + ps * kPStage;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = lane + 32 * i;
+                    uint16_t hi[kNProj], lo[kNProj];
+                    const float* f = reinterpret_cast<const float*>(&pr[i][0]);
+#pragma unroll
+                    for (int j = 0; j < kNProj; ++j) split_tf32(tf32_rna(f[j]), hi[j], lo[j]);
+                    const uint16_t* src[6] = {hi, hi + 8, lo, lo + 8, hi + 16, lo + 16};
+#pragma unroll
+                    for (int jb = 0; jb < 6; ++jb) {
+                        uint4 v;
+                        v.x = src[jb][0] | ((uint32_t)src[jb][1] << 16);
+                        v.y = src[jb][2] | ((uint32_t)src[jb][3] << 16);
+                        v.z = src[jb][4] | ((uint32_t)src[jb][5] << 16);
+                        v.w = src[jb][6] | ((uint32_t)src[jb][7] << 16);
+                        *reinterpret_cast<uint4*>(psm + p_off(tok, jb)) = v;
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(C::B_PF + ps));
+                if (++ps == NP) { ps = 0; pph ^= 1u; }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                  // TMEM lane quarter = token rows 32q..32q+31
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int rr = q * 32 + lane;            // row within the token tile
+        const float Kf = static_cast<float>(p.K);
+        const uint64_t pol = ptx::policy_evict_first();
+        int xs = 0, ab = 0, local = 0;
+        uint32_t xph = 0, aph = 0;
+        int pend = -1;                           // stage whose dX stores may still read smem
+        bool ok = true;
+        for (int it = it_begin; it < it_end && ok; ++it, ++local) {
+            const Item I = item_at(p, it);
+            const int db = local & 1;
+            const uint32_t dph = (uint32_t)(local >> 1) & 1u;
+            for (int tt = 0; tt < I.ntiles; ++tt) {
+                const int tok0 = I.t_begin + tt * kTokenTile;
+                const int row = tok0 + rr;
+                float c = 0.f;
+                if (row < p.T) c = __ldg(p.grad_r + row) / (__ldg(p.r + row) * Kf);
+                if (!wait_bar(bar(C::B_AF + ab), aph, abort_flag, p.status, tmo, true) ||
+                    !wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                uint8_t* xst = smem + (uint32_t)xs * C::stage_bytes;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint8_t* xrow = xst + h * kBoxBytes + rr * 128;
+                    const uint8_t* arow = xst + kXTile + h * kBoxBytes + rr * 128;
+#pragma unroll
+                    for (int sub = 0; sub < 2; ++sub) {
+                        uint32_t v[32];
+                        ptx::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)ab * kStrip +
+                                                    (uint32_t)(h * 64 + sub * 32), v);
+                        ptx::tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int ch = sub * 4 + i;
+                            const uint32_t off = (uint32_t)((ch ^ (rr & 7)) << 4);
+                            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + off);
+                            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 = __uint_as_float(xw[e] << 16);
+                                const float x1 = __uint_as_float(xw[e] & 0xFFFF0000u);
+                                const float d0 = fmaf(c, x0, __uint_as_float(v[i * 8 + 2 * e]));
+                                const float d1 = fmaf(c, x1, __uint_as_float(v[i * 8 + 2 * e + 1]));
+                                o[e] = pack_bf16x2(d0, d1);
+                            }
+                            if (ADD) {
+                                const uint4 av = *reinterpret_cast<const uint4*>(arow + off);
+                                const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float s0 = __uint_as_float(o[e] << 16) + __uint_as_float(aw[e] << 16);
+                                    const float s1 = __uint_as_float(o[e] & 0xFFFF0000u) +
+                                                     __uint_as_float(aw[e] & 0xFFFF0000u);
+                                    o[e] = pack_bf16x2(s0, s1);
+                                }
+                            }
+                            *reinterpret_cast<uint4*>(xrow + off) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && tok0 + q * 32 < p.T && I.col0 + h * kBoxCols < p.K)
+                        ptx::tma_store_2d(&dx_map, ptx::smem_u32(xst + h * kBoxBytes + q * 32 * 128),
+                                          I.col0 + h * kBoxCols, tok0 + q * 32, pol);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(bar(C::B_AE + ab));
+                    ptx::bulk_commit();
+                    if (pend >= 0) {
+                        ptx::bulk_wait_read<1>();      // the previous tile's stores have read smem
+                        ptx::mbar_arrive(bar(C::B_XE + pend));
+                    }
+                }
+                pend = xs;
+                if (++xs == NS) { xs = 0; xph ^= 1u; }
+                if (++ab == 2) { ab = 0; aph ^= 1u; }
+            }
+            if (!ok) break;
+            // dW partial of this chunk: lane = column of the strip
+            if (!wait_bar(bar(C::B_DF + db), dph, abort_flag, p.status, tmo, true)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t d0[16], d1[16], d2[16];
+            const uint32_t dcol = tmem + lane_base + kDwCol + (uint32_t)db * kDwColStride;
+            ptx::tmem_ld_32x32b_x16(dcol, d0);
+            ptx::tmem_ld_32x32b_x16(dcol + 16, d1);
+            ptx::tmem_ld_32x32b_x16(dcol + 32, d2);
+            ptx::tc_wait_ld();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(C::B_DE + db));
+            const int col = I.col0 + q * 32 + lane;
+            if (col < p.K) {
+                float* dst = p.partial + (size_t)I.chunk * kNProj * p.K + col;
+                // accumulator columns: 0-15 X^T Ph[0..15], 16-31 X^T Pl[0..15],
+                //                      32-39 X^T Ph[16..23], 40-47 X^T Pl[16..23]
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    dst[(size_t)j * p.K] = __uint_as_float(d0[j]) + __uint_as_float(d1[j]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[(size_t)(16 + i) * p.K] = __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]);
+            }
+        }
+        if (lane == 0) ptx::bulk_wait<0>();   // all dX stores of this warp are complete
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t smem_bytes(bool has_addend) {
+    return has_addend ? Cfg<true>::alloc : Cfg<false>::alloc;
+}
+
+cudaError_t setup(bool has_addend) {
+    if (has_addend)
+        return cudaFuncSetAttribute(main_tc_kernel<true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)Cfg<true>::alloc);
+    return cudaFuncSetAttribute(main_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Cfg<false>::alloc);
+}
+
+cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensorMap& dx_map,
+                   const CUtensorMap& add_map, int grid, cudaStream_t stream) {
+    if (p.addend != nullptr)
+        main_tc_kernel<true><<<grid, kThreads, Cfg<true>::alloc, stream>>>(p, x_map, dx_map, add_map);
+    else
+        main_tc_kernel<false><<<grid, kThreads, Cfg<false>::alloc, stream>>>(p, x_map, dx_map,
+                                                                             add_map);
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace mhcpb

@@ -1,0 +1,88 @@
+"""Host-only checks of the C-ABI library: it loads without a GPU, exports every
+function ``include/mhcpb.h`` declares, and rejects bad flags and shapes before
+making any CUDA call (the cuDNN frontend page "DSv4.1 mHC projection/RMS
+backward", "Requirements and tensor contract": other shapes and precisions are
+rejected; allow_tf32 must be passed explicitly)."""
+import os
+import re
+
+import pytest
+
+from rms_backward_gb300 import abi
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mhcpb.h")
+
+
+def _built():
+    return os.path.exists(abi.LIB_PATH)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not _built():
+        from rms_backward_gb300 import build
+        try:
+            build.build()
+        except RuntimeError as e:  # pragma: no cover
+            pytest.skip(f"cannot build libmhcpb.so here: {e}")
+    return abi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(mhcpb_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcpb_destroy"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(abi.EXPORTED) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for s in range(0, 11):
+        assert abi.status_string(s)
+    assert abi.status_string(12345) == "unknown status"
+
+
+@pytest.mark.parametrize("T,K,flags,status", [
+    (100, 512, 0, abi.MHCPB_ERR_TF32_NOT_ALLOWED),
+    (100, 512, abi.MHCPB_HAS_ADDEND, abi.MHCPB_ERR_TF32_NOT_ALLOWED),
+    (100, 512, abi.MHCPB_ALLOW_TF32 | 64, abi.MHCPB_ERR_INVALID_ARG),
+    (0, 512, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
+    (-5, 512, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
+    (100, 0, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
+    (100, 12, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
+    (100, 4, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
+    ((1 << 24) + 1, 512, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
+    (100, (1 << 20) + 8, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
+])
+def test_plan_create_rejects_before_cuda(lib, T, K, flags, status):
+    with pytest.raises(abi.MhcpbError) as ei:
+        abi.mhcpb_plan_create(T, K, 0, flags)
+    assert ei.value.status == status
+
+
+def test_null_arguments_rejected(lib):
+    import ctypes
+    assert lib.mhcpb_plan_create(None, 10, 16, 0, 1) == abi.MHCPB_ERR_INVALID_ARG
+    assert lib.mhcpb_workspace_bytes(None, None) == abi.MHCPB_ERR_INVALID_ARG
+    assert lib.mhcpb_execute(None, *([None] * 8), 0, None, None) == abi.MHCPB_ERR_INVALID_ARG
+    assert lib.mhcpb_plan_query(None, 0, None) == abi.MHCPB_ERR_INVALID_ARG
+    assert lib.mhcpb_destroy(None) == abi.MHCPB_OK
+    v = ctypes.c_int()
+    assert lib.mhcpb_get_device_status(None, ctypes.byref(v), 0) == abi.MHCPB_ERR_INVALID_ARG
+
+
+def test_workspace_formula_matches_page_size():
+    # S * 24 * K * 4 with S = ceil(T / 512): 15,728,640 bytes at T=4096, K=20480,
+    # the workspace size the page states for the training profile.
+    T, K = 4096, 20480
+    S = -(-T // abi.MHCPB_TOKENS_PER_PARTIAL)
+    assert S * 24 * K * 4 == 15_728_640

@@ -1,0 +1,99 @@
+"""Determinism and stream/graph behaviour of the CUDA path.
+
+The page fixes the partial-dW reduction to a fixed order without atomics
+(cuDNN frontend page "DSv4.1 mHC projection/RMS backward", intro), execution is
+stream-ordered and graph-capturable ("Prepared class API").  dW (and dX) must
+be bitwise identical across repeated executes, across streams and across graph
+replays.
+"""
+import numpy as np
+import pytest
+import torch
+
+from rms_backward_gb300 import workloads as WL
+
+from gpu_helpers import Runner
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(r):
+    dx, dw = r.results()
+    return dx.copy(), dw.view(np.uint32).copy()
+
+
+@pytest.mark.parametrize("fma", [False, True], ids=["tcgen05", "fma"])
+def test_repeated_executes_bitwise(fma):
+    wl = WL.make("det", T=2000, K=4096, seed=30)
+    r = Runner(wl, fma_kernel=fma)
+    r.run()
+    dx0, dw0 = _bits(r)
+    for _ in range(20):
+        r.run()
+    for _ in range(3):
+        r.dw.fill_(float("nan"))
+        r.run()
+        dx, dw = _bits(r)
+        assert np.array_equal(dx, dx0) and np.array_equal(dw, dw0)
+    r.plan.close()
+
+
+def test_training_profile_repeats_bitwise():
+    wl = WL.config("training_profile")
+    r = Runner(wl)
+    r.run()
+    dx0, dw0 = _bits(r)
+    for _ in range(5):
+        r.run()
+    dx, dw = _bits(r)
+    assert np.array_equal(dw, dw0) and np.array_equal(dx, dx0)
+    r.plan.close()
+
+
+def test_side_stream_matches_default():
+    wl = WL.make("det", T=1500, K=2048, seed=31)
+    r = Runner(wl)
+    r.run()
+    dx0, dw0 = _bits(r)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        r.dw.fill_(0)
+        r.run(stream=s)
+    s.synchronize()
+    dx, dw = _bits(r)
+    assert np.array_equal(dx, dx0) and np.array_equal(dw, dw0)
+    r.plan.close()
+
+
+@pytest.mark.parametrize("addend", [False, True])
+def test_cuda_graph_capture_and_replay(addend):
+    wl = WL.make("graph", T=1200, K=3072, seed=32, addend=addend)
+    r = Runner(wl)
+    r.run()
+    dx0, dw0 = _bits(r)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        r.run(stream=s)
+    for _ in range(3):
+        r.dx.fill_(0)
+        r.dw.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        dx, dw = _bits(r)
+        assert np.array_equal(dx, dx0) and np.array_equal(dw, dw0)
+    r.plan.close()
+
+
+def test_independent_plans_same_shape_agree():
+    wl = WL.make("det", T=900, K=1536, seed=33)
+    a, b = Runner(wl), Runner(wl)
+    a.run()
+    b.run()
+    da, wa = _bits(a)
+    db, wb = _bits(b)
+    assert np.array_equal(da, db) and np.array_equal(wa, wb)
+    a.plan.close()
+    b.plan.close()
