@@ -49,6 +49,8 @@ def _args():
     ap.add_argument("--kernel", choices=["tcgen05", "fma"], default="tcgen05")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="warm-up and timed steps only (for profiler runs); prints a short line")
     return ap.parse_args()
 
 
@@ -271,6 +273,21 @@ def run_ours(args):
     torch.cuda.synchronize()
     if plan.device_status() != 0:
         raise RuntimeError("device-side timeout during warm-up")
+
+    if args.quick:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / max(1, args.steps)
+        if rank == 0:
+            print(json.dumps({"quick": True, "kernel": args.kernel, "steps": args.steps,
+                              "ms_per_step_no_flush": ms}), flush=True)
+        status = plan.device_status()
+        plan.close()
+        return 0 if status == 0 else 1
 
     clocks = ClockSampler(local)
     clocks.start()

@@ -28,10 +28,10 @@ def _bufs(addend=False):
     return b
 
 
-def _exec(plan, b, ws, **over):
+def _exec(plan, b, wsbuf, **over):
     args = dict(x=b["x"].data_ptr(), w=b["w"].data_ptr(), gp=b["gp"].data_ptr(),
                 gr=b["gr"].data_ptr(), r=b["r"].data_ptr(), dx=b["dx"].data_ptr(),
-                dw=b["dw"].data_ptr(), ws=ws.data_ptr(), wsb=ws.numel(),
+                dw=b["dw"].data_ptr(), ws=wsbuf.data_ptr(), wsb=wsbuf.numel(),
                 add=None if b["add"] is None else b["add"].data_ptr())
     args.update(over)
     abi.mhcpb_execute(plan.handle, args["x"], args["w"], args["gp"], args["gr"], args["r"],
