@@ -327,7 +327,11 @@ def run_ours(args):
     k1, k2 = [], []
     for i in range(min(200, args.steps)):
         flush.fill_(1.0)
+        # torch only knows an event was recorded if it recorded it itself; the
+        # library then re-records the same handles at the kernel boundaries
         e0.record(stream)
+        e1.record(stream)
+        e2.record(stream)
         st = lib.mhcpb_execute_profiled(
             plan.handle, x.data_ptr(), w.data_ptr(), gp.data_ptr(), gr.data_ptr(), r.data_ptr(),
             dx.data_ptr(), dw.data_ptr(), ws.data_ptr(), plan.workspace_bytes, None, sh,

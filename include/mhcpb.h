@@ -83,7 +83,13 @@ enum {
     /* Use the FP32-FMA (CUDA-core) streaming kernel instead of the tensor-core
      * one.  Same results within tolerance, same determinism; kept as the
      * measured control for the tensor-core kernel. */
-    MHCPB_FMA_KERNEL = 4u
+    MHCPB_FMA_KERNEL = 4u,
+    /* Test hook for failure detection: in the tensor-core kernel the MMA
+     * issuer first waits on a barrier that nothing completes, so the execute
+     * ends by the in-kernel wait limit, records MHCPB_ERR_DEVICE_TIMEOUT in the
+     * status word and leaves the context usable.  Outputs are undefined.  Not
+     * for production use. */
+    MHCPB_TEST_INJECT_STALL = 1u << 30
 };
 
 /* Shape limits (inclusive). */
@@ -143,6 +149,12 @@ mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status
  * 3 grid size of the streaming kernel, 4 flags, 5 streaming-kernel dynamic
  * shared memory bytes, 6 token tile, 7 column strip width. */
 mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value);
+
+/* Sets the bound on every wait inside the plan's kernels (default 1 s,
+ * accepted range 1 ms .. 60 s).  A wait that runs out ends the kernel early
+ * with MHCPB_ERR_DEVICE_TIMEOUT in the status word.  Applies to executes
+ * enqueued after the call. */
+mhcpb_status_t mhcpb_plan_set_wait_limit(mhcpb_plan_t plan, uint64_t nanoseconds);
 
 /* Releases the plan (and its status word).  Safe on NULL. */
 mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan);

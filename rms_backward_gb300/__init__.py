@@ -16,7 +16,7 @@ from . import abi
 from .abi import (  # noqa: F401
     MHCPB_ALLOW_TF32, MHCPB_FMA_KERNEL, MHCPB_HAS_ADDEND, MhcpbError, mhcpb_destroy,
     mhcpb_execute, mhcpb_get_device_status, mhcpb_last_cuda_error, mhcpb_plan_create,
-    mhcpb_plan_query, mhcpb_status_string, mhcpb_workspace_bytes,
+    mhcpb_plan_query, mhcpb_plan_set_wait_limit, mhcpb_status_string, mhcpb_workspace_bytes,
 )
 
 
@@ -24,8 +24,10 @@ class Plan:
     """A prepared backward for one (T, K) on one device (owns a C plan handle)."""
 
     def __init__(self, T: int, K: int, device: int = 0, *, addend: bool = False,
-                 fma_kernel: bool = False):
+                 fma_kernel: bool = False, test_inject_stall: bool = False):
         flags = abi.MHCPB_ALLOW_TF32
+        if test_inject_stall:
+            flags |= abi.MHCPB_TEST_INJECT_STALL
         if addend:
             flags |= abi.MHCPB_HAS_ADDEND
         if fma_kernel:
@@ -33,6 +35,9 @@ class Plan:
         self.T, self.K, self.device, self.flags = int(T), int(K), int(device), flags
         self.handle = mhcpb_plan_create(T, K, device, flags)
         self.workspace_bytes = mhcpb_workspace_bytes(self.handle)
+
+    def set_wait_limit(self, nanoseconds: int) -> None:
+        mhcpb_plan_set_wait_limit(self.handle, nanoseconds)
 
     def query(self, which: str) -> int:
         return mhcpb_plan_query(self.handle, which)

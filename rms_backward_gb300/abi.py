@@ -28,6 +28,7 @@ MHCPB_ERR_UNSUPPORTED_DEVICE = 10
 MHCPB_ALLOW_TF32 = 1
 MHCPB_HAS_ADDEND = 2
 MHCPB_FMA_KERNEL = 4
+MHCPB_TEST_INJECT_STALL = 1 << 30
 
 MHCPB_NPROJ = 24
 MHCPB_GRAD_PROJ_COLS = 32
@@ -36,8 +37,8 @@ MHCPB_TOKENS_PER_PARTIAL = 512
 QUERY = {"T": 0, "K": 1, "S": 2, "grid": 3, "flags": 4, "smem": 5, "token_tile": 6, "strip": 7}
 
 EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcpb_execute_profiled",
-            "mhcpb_get_device_status", "mhcpb_plan_query", "mhcpb_destroy",
-            "mhcpb_status_string", "mhcpb_last_cuda_error")
+            "mhcpb_get_device_status", "mhcpb_plan_query", "mhcpb_plan_set_wait_limit",
+            "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error")
 
 
 class MhcpbError(RuntimeError):
@@ -69,13 +70,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_execute_profiled.argtypes = [P, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P]
     lib.mhcpb_get_device_status.argtypes = [P, ctypes.POINTER(I32), I32]
     lib.mhcpb_plan_query.argtypes = [P, I32, ctypes.POINTER(I64)]
+    lib.mhcpb_plan_set_wait_limit.argtypes = [P, ctypes.c_uint64]
     lib.mhcpb_destroy.argtypes = [P]
     lib.mhcpb_status_string.argtypes = [I32]
     lib.mhcpb_status_string.restype = ctypes.c_char_p
     lib.mhcpb_last_cuda_error.argtypes = []
     lib.mhcpb_last_cuda_error.restype = ctypes.c_char_p
     for name in ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute",
-                 "mhcpb_execute_profiled", "mhcpb_get_device_status", "mhcpb_plan_query", "mhcpb_destroy"):
+                 "mhcpb_execute_profiled", "mhcpb_get_device_status", "mhcpb_plan_query",
+                 "mhcpb_plan_set_wait_limit", "mhcpb_destroy"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -124,6 +127,10 @@ def mhcpb_plan_query(plan: int, which) -> int:
     code = QUERY[which] if isinstance(which, str) else int(which)
     _check(load().mhcpb_plan_query(plan, code, ctypes.byref(v)), "mhcpb_plan_query")
     return v.value
+
+
+def mhcpb_plan_set_wait_limit(plan: int, nanoseconds: int) -> None:
+    _check(load().mhcpb_plan_set_wait_limit(plan, int(nanoseconds)), "mhcpb_plan_set_wait_limit")
 
 
 def mhcpb_destroy(plan: int) -> None:

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -27,6 +28,7 @@ struct mhcpb_plan_s {
     size_t smem = 0;
     uint32_t* d_status = nullptr;
     uint64_t timeout_ns = 1000000000ull;  // 1 s bound on every in-kernel wait
+    int epi_warps = 8;    // epilogue warps of the tensor-core kernel (4 or 8)
 };
 
 namespace {
@@ -85,6 +87,29 @@ bool encode_bf16_map(CUtensorMap* m, const void* base, int64_t T, int64_t K, uin
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// FP32 tensor maps without swizzle: grad_proj [T, 32] read as boxes of 24
+// columns x 128 rows (columns 24..31 are never fetched), and [T] vectors read
+// as boxes of 128.
+bool encode_f32_map(CUtensorMap* m, const void* base, int64_t T, int cols, uint32_t box_cols,
+                    uint32_t box_rows) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    const cuuint32_t estr[2] = {1, 1};
+    if (cols == 0) {
+        const cuuint64_t dims[1] = {(cuuint64_t)T};
+        const cuuint32_t box[1] = {box_rows};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<void*>(base), dims, nullptr,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Range {
     uintptr_t lo, hi;
 };
@@ -129,7 +154,8 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
                                  uint32_t flags) {
     if (out == nullptr) return MHCPB_ERR_INVALID_ARG;
     if ((flags & MHCPB_ALLOW_TF32) == 0) return MHCPB_ERR_TF32_NOT_ALLOWED;
-    if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND | MHCPB_FMA_KERNEL)) != 0)
+    if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND | MHCPB_FMA_KERNEL |
+                            MHCPB_TEST_INJECT_STALL)) != 0)
         return MHCPB_ERR_INVALID_ARG;
     if (T < 1 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
         return MHCPB_ERR_UNSUPPORTED_SHAPE;
@@ -155,7 +181,6 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
         if ((e = fma::setup()) != cudaSuccess) return cuda_fail(e, "setup (FMA kernel)");
     } else {
         if (!get_encode()) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
-        if ((e = tc::setup(add)) != cudaSuccess) return cuda_fail(e, "setup (tensor-core kernel)");
     }
 
     mhcpb_plan_s* p = new mhcpb_plan_s();
@@ -173,7 +198,12 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
         p->n_strips = (int)((K + tc::kStrip - 1) / tc::kStrip);
         const int64_t items = (int64_t)p->n_strips * p->S;
         p->grid = (int)(items < sms ? items : sms);
-        p->smem = tc::smem_bytes(add);
+        if (const char* ev = std::getenv("MHCPB_EPI_WARPS")) p->epi_warps = std::atoi(ev) == 4 ? 4 : 8;
+        if ((e = tc::setup(add, p->epi_warps)) != cudaSuccess) {
+            delete p;
+            return cuda_fail(e, "setup (tensor-core kernel)");
+        }
+        p->smem = tc::smem_bytes(add, p->epi_warps);
     }
     if ((e = cudaMalloc(&p->d_status, sizeof(uint32_t))) != cudaSuccess) {
         delete p;
@@ -262,6 +292,7 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float
     p.partial = static_cast<float*>(workspace);
     p.status = plan->d_status;
     p.timeout_ns = plan->timeout_ns;
+    p.test_flags = (plan->flags & MHCPB_TEST_INJECT_STALL) ? kTestInjectStall : 0u;
 
     cudaError_t e;
     if (ev0 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev0), st)) != cudaSuccess)
@@ -270,11 +301,14 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float
         e = fma::launch(p, st);
         if (e != cudaSuccess) return cuda_fail(e, "launch (FMA kernel)");
     } else {
-        CUtensorMap xm, dxm, am;
+        CUtensorMap xm, dxm, am, gpm, grm, rm;
         if (!encode_bf16_map(&xm, x, T, K, tc::kTokenTile) || !encode_bf16_map(&dxm, dx, T, K, 32) ||
-            !encode_bf16_map(&am, add ? grad_x_addend : x, T, K, tc::kTokenTile))
+            !encode_bf16_map(&am, add ? grad_x_addend : x, T, K, tc::kTokenTile) ||
+            !encode_f32_map(&gpm, grad_proj, T, kGradProjCols, kNProj, tc::kTokenTile) ||
+            !encode_f32_map(&grm, grad_r, T, 0, 0, tc::kTokenTile) ||
+            !encode_f32_map(&rm, r, T, 0, 0, tc::kTokenTile))
             return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-        e = tc::launch(p, xm, dxm, am, plan->grid, st);
+        e = tc::launch(p, xm, dxm, am, gpm, grm, rm, plan->grid, plan->epi_warps, st);
         if (e != cudaSuccess) return cuda_fail(e, "launch (tensor-core kernel)");
     }
     if (ev1 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev1), st)) != cudaSuccess)
@@ -317,6 +351,13 @@ mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     }
     *status = static_cast<mhcpb_status_t>(v);
+    return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_plan_set_wait_limit(mhcpb_plan_t plan, uint64_t nanoseconds) {
+    if (plan == nullptr) return MHCPB_ERR_INVALID_ARG;
+    if (nanoseconds < 1000000ull || nanoseconds > 60000000000ull) return MHCPB_ERR_INVALID_ARG;
+    plan->timeout_ns = nanoseconds;
     return MHCPB_OK;
 }
 

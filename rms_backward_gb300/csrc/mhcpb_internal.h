@@ -30,18 +30,23 @@ struct MainParams {
     float* partial;       // [S, 24, K]
     uint32_t* status;     // device status word
     uint64_t timeout_ns;  // bound on every wait inside the kernel
+    uint32_t test_flags;  // kTestInjectStall: the MMA issuer waits on a barrier nothing completes
 };
+
+constexpr uint32_t kTestInjectStall = 1u;
 
 // Tensor-core (tcgen05 + TMA) streaming kernel: geometry and launch.
 namespace tc {
 constexpr int kTokenTile = 128;    // MMA M for dX; K-extent of one dW MMA group
 constexpr int kStrip = 128;        // columns per strip: MMA N for dX, M for dW
 constexpr int kBoxCols = 64;       // TMA box width (128 bytes of BF16)
-constexpr int kThreads = 256;
-size_t smem_bytes(bool has_addend);
-cudaError_t setup(bool has_addend);
+size_t smem_bytes(bool has_addend, int epi_warps);
+cudaError_t setup(bool has_addend, int epi_warps);
+// Tensor maps: x/dx/addend BF16 [T,K] boxes 64 x {128,32,128} (128-byte swizzle),
+// grad_proj FP32 [T,32] box 24 x 128, grad_r and r FP32 [T] boxes of 128.
 cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensorMap& dx_map,
-                   const CUtensorMap& add_map, int grid, cudaStream_t stream);
+                   const CUtensorMap& add_map, const CUtensorMap& gp_map, const CUtensorMap& gr_map,
+                   const CUtensorMap& r_map, int grid, int epi_warps, cudaStream_t stream);
 }  // namespace tc
 
 // FP32-FMA (CUDA core) streaming kernel: the measured control.

@@ -12,9 +12,11 @@
 //    strip, 512-token chunk) pairs in strip-major order; a CTA takes a
 //    contiguous range of them, so W for a strip is staged once per strip.
 //    The chunking depends only on T, so dW bits do not depend on the SM count.
-//  * X arrives by TMA in 128-token x 128-column tiles (two 64-column boxes,
-//    128-byte swizzle) into a ring of shared-memory stages; X is read from
-//    HBM exactly once.
+//  * One pipeline stage per 128-token tile, filled by TMA: the X tile
+//    (128 x 128 BF16 as two 64-column boxes, 128-byte swizzle, read from HBM
+//    exactly once, L2 evict-first), the tile's 24 used grad_proj columns and
+//    its grad_r and r (L2 evict-last: every strip re-reads them), and with the
+//    fused addend its BF16 addend tile.
 //  * Both contractions run on the tensor cores (tcgen05.mma kind::f16, BF16
 //    operands, FP32 accumulators in TMEM).  A TF32 value has 11 significant
 //    bits, so it is exactly hi + lo with hi, lo BF16 (hi = bf16(v),
@@ -23,14 +25,15 @@
 //        dX tile  = [Ph Pl] x [Wh; Wh] + [Ph Pl] x [Wl; Wl]      (M128 N128 K96)
 //        dW^T     = X^T x [Ph Pl]   (X used in place, MN-major; M128 N48 K128)
 //    X itself is BF16, a subset of TF32, and needs no conversion.
-//  * Four epilogue warps read the dX accumulator from TMEM, add c*X (FP32 FMA,
-//    X from the same shared-memory tile), round to BF16 (and add the optional
-//    BF16 addend the way a separate BF16 add would), write the result over
-//    the X tile in place and TMA-store it.  At the end of each chunk they
-//    write the chunk's dW partial (hi and lo halves summed) to the workspace.
+//  * Epilogue warps read the dX accumulator from TMEM (double-buffered loads),
+//    add c*X (FP32 FMA, X from the same shared-memory tile), round to BF16
+//    (and add the optional BF16 addend the way a separate BF16 add would),
+//    write the result over the X tile in place and TMA-store it.  At the end
+//    of each chunk they write the chunk's dW partial (hi and lo halves summed)
+//    to the workspace.
 //  * Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2 operand
 //    preparation (TF32 rounding and BF16 hi/lo split of P and W into the
-//    tensor-core operand layout), 4-7 epilogue.
+//    tensor-core operand layout, from shared memory), 3 idle, 4.. epilogue.
 //  * Every mbarrier wait is bounded (see wait_bar): on timeout the kernel
 //    records a status word, drains its own copies and MMAs and exits.
 #include <cuda_bf16.h>
@@ -44,20 +47,28 @@ namespace tc {
 namespace {
 
 constexpr int kChunk = kTokensPerPartial;
-constexpr int kNJS = 2 * kNProj;                         // 48 split P columns
-constexpr uint32_t kXTile = kTokenTile * kStrip * 2;     // 32 KiB of BF16
+constexpr int kNJS = 2 * kNProj;                           // 48 split P columns
+constexpr uint32_t kXTile = kTokenTile * kStrip * 2;       // 32 KiB of BF16
 constexpr uint32_t kBoxBytes = kTokenTile * kBoxCols * 2;  // 16 KiB (one 64-column box)
-constexpr uint32_t kPStage = kTokenTile * kNJS * 2;      // 12 KiB
-constexpr uint32_t kWBytes = kStrip * 64 * 2;            // 16 KiB (8 blocks of 8 per column group)
+constexpr uint32_t kPRaw = kTokenTile * kNProj * 4;        // 12 KiB: 128 rows x 24 FP32
+constexpr uint32_t kPStage = kTokenTile * kNJS * 2;        // 12 KiB split P
+constexpr uint32_t kWBytes = kStrip * 64 * 2;              // 16 KiB (8 blocks of 8 per column group)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDwCol = 256;                         // dW accumulators at 256 and 320
+constexpr uint32_t kDwCol = 256;                           // dW accumulators at 256 and 320
 constexpr uint32_t kDwColStride = 64;
 
-template <bool ADD>
+template <bool ADD, int NEPI>
 struct Cfg {
-    static constexpr int NS = ADD ? 3 : 5;               // X (+addend) stages
-    static constexpr int NP = ADD ? 1 : 2;               // split-P stages
-    static constexpr uint32_t stage_bytes = ADD ? 2 * kXTile : kXTile;
+    static constexpr int NS = ADD ? 2 : 4;                 // pipeline stages
+    static constexpr int NP = 2;                           // split-P stages
+    static constexpr int HPW = 8 / NEPI;                   // 64-column boxes per epilogue warp
+    static constexpr int threads = (4 + NEPI) * 32;
+    // stage: X | raw P [128][24] | grad_r[128] | r[128] | addend (1 KiB-aligned parts)
+    static constexpr uint32_t st_p = kXTile;
+    static constexpr uint32_t st_gr = st_p + kPRaw;
+    static constexpr uint32_t st_r = st_gr + kTokenTile * 4;
+    static constexpr uint32_t st_add = st_r + kTokenTile * 4;
+    static constexpr uint32_t stage_bytes = st_add + (ADD ? kXTile : 0u);
     static constexpr uint32_t off_p = NS * stage_bytes;
     static constexpr uint32_t off_w = off_p + NP * kPStage;
     static constexpr uint32_t off_bar = off_w + kWBytes;
@@ -69,7 +80,10 @@ struct Cfg {
     static constexpr int n_bars = B_FIN + 1;
     static constexpr uint32_t off_misc = off_bar + n_bars * 8;
     static constexpr uint32_t bytes = off_misc + 16;
-    static constexpr uint32_t alloc = bytes + 1024;      // room to align the base to 1 KiB
+    static constexpr uint32_t alloc = bytes + 1024;        // room to align the base to 1 KiB
+    static_assert(st_add % 1024 == 0, "swizzled addend tile must be 1 KiB aligned");
+    static_assert(stage_bytes % 1024 == 0, "stages must stay 1 KiB aligned");
+    static_assert(alloc <= 232448, "shared memory budget");
 };
 
 // Bounded mbarrier wait.  Returns false when the CTA is aborting (another role
@@ -115,6 +129,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint4 pack8(const uint16_t* s) {
+    uint4 v;
+    v.x = s[0] | ((uint32_t)s[1] << 16);
+    v.y = s[2] | ((uint32_t)s[3] << 16);
+    v.z = s[4] | ((uint32_t)s[5] << 16);
+    v.w = s[6] | ((uint32_t)s[7] << 16);
+    return v;
+}
+
 // Work-item geometry shared by all roles.
 struct Item {
     int strip, chunk, col0, t_begin, ntiles;
@@ -147,12 +170,49 @@ __device__ __forceinline__ uint32_t w_off(int col, int wb) {
     return (uint32_t)(((col >> 3) * 8 + wb) * 128 + (col & 7) * 16);
 }
 
+struct Maps {
+    CUtensorMap x, dx, add, gp, gr, r;
+};
+
+// One 32-column chunk of the dX epilogue for this thread's row: acc (from
+// TMEM) + c * x, BF16 rounding, optional BF16 addend, written over x in place.
 template <bool ADD>
-__global__ void __launch_bounds__(kThreads, 1)
-    main_tc_kernel(const MainParams p, const __grid_constant__ CUtensorMap x_map,
-                   const __grid_constant__ CUtensorMap dx_map,
-                   const __grid_constant__ CUtensorMap add_map) {
-    using C = Cfg<ADD>;
+__device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], float c, uint8_t* xrow,
+                                          const uint8_t* arow, int rr, int sub) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int ch = sub * 4 + i;
+        const uint32_t off = (uint32_t)((ch ^ (rr & 7)) << 4);
+        const uint4 xv = *reinterpret_cast<const uint4*>(xrow + off);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x0 = __uint_as_float(xw[e] << 16);
+            const float x1 = __uint_as_float(xw[e] & 0xFFFF0000u);
+            const float d0 = fmaf(c, x0, __uint_as_float(v[i * 8 + 2 * e]));
+            const float d1 = fmaf(c, x1, __uint_as_float(v[i * 8 + 2 * e + 1]));
+            o[e] = pack_bf16x2(d0, d1);
+        }
+        if (ADD) {
+            const uint4 av = *reinterpret_cast<const uint4*>(arow + off);
+            const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float s0 = __uint_as_float(o[e] << 16) + __uint_as_float(aw[e] << 16);
+                const float s1 =
+                    __uint_as_float(o[e] & 0xFFFF0000u) + __uint_as_float(aw[e] & 0xFFFF0000u);
+                o[e] = pack_bf16x2(s0, s1);
+            }
+        }
+        *reinterpret_cast<uint4*>(xrow + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+template <bool ADD, int NEPI>
+__global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
+    main_tc_kernel(const MainParams p, const __grid_constant__ Maps maps) {
+    using C = Cfg<ADD, NEPI>;
     constexpr int NS = C::NS, NP = C::NP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -171,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(bar(C::B_XF + s), 1);
-            ptx::mbar_init(bar(C::B_XE + s), 4);
+            ptx::mbar_init(bar(C::B_XE + s), NEPI);
         }
         for (int s = 0; s < NP; ++s) {
             ptx::mbar_init(bar(C::B_PF + s), 1);
@@ -179,9 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(C::B_AF + b), 1);
-            ptx::mbar_init(bar(C::B_AE + b), 4);
+            ptx::mbar_init(bar(C::B_AE + b), NEPI);
             ptx::mbar_init(bar(C::B_DF + b), 1);
-            ptx::mbar_init(bar(C::B_DE + b), 4);
+            ptx::mbar_init(bar(C::B_DE + b), NEPI);
         }
         ptx::mbar_init(bar(C::B_WF), 1);
         ptx::mbar_init(bar(C::B_WE), 1);
@@ -190,9 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        ptx::prefetch_tensormap(&x_map);
-        ptx::prefetch_tensormap(&dx_map);
-        if (ADD) ptx::prefetch_tensormap(&add_map);
+        ptx::prefetch_tensormap(&maps.x);
+        ptx::prefetch_tensormap(&maps.dx);
+        ptx::prefetch_tensormap(&maps.gp);
+        ptx::prefetch_tensormap(&maps.gr);
+        ptx::prefetch_tensormap(&maps.r);
+        if (ADD) ptx::prefetch_tensormap(&maps.add);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
@@ -209,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol = ptx::policy_evict_first();
+            const uint64_t pol_stream = ptx::policy_evict_first();
+            const uint64_t pol_keep = ptx::policy_evict_last();
             int st = 0;
             uint32_t ph = 0;
             uint32_t issued = 0, last_par = 0;
@@ -223,15 +287,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int tok0 = I.t_begin + tt * kTokenTile;
                     const uint32_t dst = sbase + (uint32_t)st * C::stage_bytes;
-                    ptx::mbar_arrive_expect_tx(bar(C::B_XF + st), C::stage_bytes);
-                    ptx::tma_load_2d(dst, &x_map, I.col0, tok0, bar(C::B_XF + st), pol);
-                    ptx::tma_load_2d(dst + kBoxBytes, &x_map, I.col0 + kBoxCols, tok0,
-                                     bar(C::B_XF + st), pol);
+                    const uint32_t fb = bar(C::B_XF + st);
+                    ptx::mbar_arrive_expect_tx(fb, C::stage_bytes);
+                    ptx::tma_load_2d(dst, &maps.x, I.col0, tok0, fb, pol_stream);
+                    ptx::tma_load_2d(dst + kBoxBytes, &maps.x, I.col0 + kBoxCols, tok0, fb,
+                                     pol_stream);
+                    ptx::tma_load_2d(dst + C::st_p, &maps.gp, 0, tok0, fb, pol_keep);
+                    ptx::tma_load_1d(dst + C::st_gr, &maps.gr, tok0, fb, pol_keep);
+                    ptx::tma_load_1d(dst + C::st_r, &maps.r, tok0, fb, pol_keep);
                     if (ADD) {
-                        ptx::tma_load_2d(dst + kXTile, &add_map, I.col0, tok0, bar(C::B_XF + st),
-                                         pol);
-                        ptx::tma_load_2d(dst + kXTile + kBoxBytes, &add_map, I.col0 + kBoxCols,
-                                         tok0, bar(C::B_XF + st), pol);
+                        ptx::tma_load_2d(dst + C::st_add, &maps.add, I.col0, tok0, fb, pol_stream);
+                        ptx::tma_load_2d(dst + C::st_add + kBoxBytes, &maps.add,
+                                         I.col0 + kBoxCols, tok0, fb, pol_stream);
                     }
                     issued |= 1u << st;
                     last_par = (last_par & ~(1u << st)) | (ph << st);
@@ -260,6 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t xph = 0, pph = 0, aph = 0;
             int n_w = 0, prev_strip = -1, local = 0;
             bool ok = true;
+            // failure-detection test hook: nothing arrives on the final barrier
+            // before the drain below, so this wait can only run out of time
+            if (p.test_flags & kTestInjectStall)
+                ok = wait_bar(bar(C::B_FIN), 0u, abort_flag, p.status, tmo, true);
             for (int it = it_begin; it < it_end && ok; ++it, ++local) {
                 const Item I = item_at(p, it);
                 const int db = local & 1;
@@ -325,37 +396,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ operand preparation
-        int ps = 0;
-        uint32_t pph = 0;
+        int xs = 0, ps = 0;
+        uint32_t xph = 0, pph = 0;
         int n_w = 0, prev_strip = -1;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item I = item_at(p, it);
             if (I.strip != prev_strip) {
+                // W columns of this lane, fetched before waiting for the buffer
+                float wv[4][kNProj];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int col = I.col0 + lane + 32 * q;
+#pragma unroll
+                    for (int j = 0; j < kNProj; ++j)
+                        wv[q][j] = col < p.K ? __ldg(p.w + (size_t)j * p.K + col) : 0.f;
+                }
                 if (n_w > 0 && !wait_bar(bar(C::B_WE), (uint32_t)(n_w - 1) & 1u, abort_flag,
                                          p.status, tmo, true)) {
                     ok = false;
                     break;
                 }
                 uint8_t* wsm = smem + C::off_w;
-                for (int cc = lane; cc < kStrip; cc += 32) {
-                    const int col = I.col0 + cc;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int cc = lane + 32 * q;
                     uint16_t hi[kNProj], lo[kNProj];
 #pragma unroll
-                    for (int j = 0; j < kNProj; ++j) {
-                        const float v = col < p.K ? tf32_rna(__ldg(p.w + (size_t)j * p.K + col)) : 0.f;
-                        split_tf32(v, hi[j], lo[j]);
-                    }
+                    for (int j = 0; j < kNProj; ++j) split_tf32(tf32_rna(wv[q][j]), hi[j], lo[j]);
                     const uint16_t* src[8] = {hi, hi + 8, hi + 16, hi + 16, lo, lo + 8, lo + 16, lo + 16};
 #pragma unroll
-                    for (int wb = 0; wb < 8; ++wb) {
-                        uint4 v;
-                        v.x = src[wb][0] | ((uint32_t)src[wb][1] << 16);
-                        v.y = src[wb][2] | ((uint32_t)src[wb][3] << 16);
-                        v.z = src[wb][4] | ((uint32_t)src[wb][5] << 16);
-                        v.w = src[wb][6] | ((uint32_t)src[wb][7] << 16);
-                        *reinterpret_cast<uint4*>(wsm + w_off(cc, wb)) = v;
-                    }
+                    for (int wb = 0; wb < 8; ++wb)
+                        *reinterpret_cast<uint4*>(wsm + w_off(cc, wb)) = pack8(src[wb]);
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -364,50 +436,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prev_strip = I.strip;
             }
             for (int tt = 0; tt < I.ntiles; ++tt) {
-                const int tok0 = I.t_begin + tt * kTokenTile;
-                // fetch this lane's four P rows before waiting for the stage
-                float4 pr[4][6];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = tok0 + lane + 32 * i;
-                    const float4* g = reinterpret_cast<const float4*>(p.grad_proj + (size_t)row * kGradProjCols);
-#pragma unroll
-                    for (int q = 0; q < 6; ++q)
-                        pr[i][q] = row < p.T ? __ldg(g + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                if (!wait_bar(bar(C::B_PE + ps), pph ^ 1u, abort_flag, p.status, tmo, true)) {
+                if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true) ||
+                    !wait_bar(bar(C::B_PE + ps), pph ^ 1u, abort_flag, p.status, tmo, true)) {
                     ok = false;
                     break;
                 }
+                const float* praw = reinterpret_cast<const float*>(smem + (uint32_t)xs * C::stage_bytes + C::st_p);
                 uint8_t* psm = smem + C::off_p + ps * kPStage;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int tok = lane + 32 * i;
+                    const int tok = lane + 32 * i;   // rows past T arrive as zeros (TMA fill)
+                    float f[kNProj];
+#pragma unroll
+                    for (int q = 0; q < 6; ++q) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(praw + tok * kNProj + 4 * q);
+                        f[4 * q] = v4.x; f[4 * q + 1] = v4.y; f[4 * q + 2] = v4.z; f[4 * q + 3] = v4.w;
+                    }
                     uint16_t hi[kNProj], lo[kNProj];
-                    const float* f = reinterpret_cast<const float*>(&pr[i][0]);
 #pragma unroll
                     for (int j = 0; j < kNProj; ++j) split_tf32(tf32_rna(f[j]), hi[j], lo[j]);
                     const uint16_t* src[6] = {hi, hi + 8, lo, lo + 8, hi + 16, lo + 16};
 #pragma unroll
-                    for (int jb = 0; jb < 6; ++jb) {
-                        uint4 v;
-                        v.x = src[jb][0] | ((uint32_t)src[jb][1] << 16);
-                        v.y = src[jb][2] | ((uint32_t)src[jb][3] << 16);
-                        v.z = src[jb][4] | ((uint32_t)src[jb][5] << 16);
-                        v.w = src[jb][6] | ((uint32_t)src[jb][7] << 16);
-                        *reinterpret_cast<uint4*>(psm + p_off(tok, jb)) = v;
-                    }
+                    for (int jb = 0; jb < 6; ++jb)
+                        *reinterpret_cast<uint4*>(psm + p_off(tok, jb)) = pack8(src[jb]);
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(C::B_PF + ps));
+                if (++xs == NS) { xs = 0; xph ^= 1u; }
                 if (++ps == NP) { ps = 0; pph ^= 1u; }
             }
         }
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
+        const int e = warp - 4;
         const int q = warp & 3;                  // TMEM lane quarter = token rows 32q..32q+31
+        const int h0 = (C::HPW == 2) ? 0 : e / 4;  // first 64-column box of this warp
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int rr = q * 32 + lane;            // row within the token tile
         const float Kf = static_cast<float>(p.K);
@@ -422,60 +487,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dph = (uint32_t)(local >> 1) & 1u;
             for (int tt = 0; tt < I.ntiles; ++tt) {
                 const int tok0 = I.t_begin + tt * kTokenTile;
-                const int row = tok0 + rr;
-                float c = 0.f;
-                if (row < p.T) c = __ldg(p.grad_r + row) / (__ldg(p.r + row) * Kf);
-                if (!wait_bar(bar(C::B_AF + ab), aph, abort_flag, p.status, tmo, true) ||
-                    !wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
+                if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* xst = smem + (uint32_t)xs * C::stage_bytes;
+                const float gr = reinterpret_cast<const float*>(xst + C::st_gr)[rr];
+                const float rv = reinterpret_cast<const float*>(xst + C::st_r)[rr];
+                const float c = (tok0 + rr < p.T) ? gr / (rv * Kf) : 0.f;
+                if (!wait_bar(bar(C::B_AF + ab), aph, abort_flag, p.status, tmo, true)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                uint8_t* xst = smem + (uint32_t)xs * C::stage_bytes;
+                const uint32_t tcol = tmem + lane_base + (uint32_t)ab * kStrip + (uint32_t)(h0 * 64);
+                uint32_t va[32], vb[32];
+                ptx::tmem_ld_32x32b_x32(tcol, va);
+                ptx::tc_wait_ld_regs(va);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int ch = 0; ch < 2 * C::HPW; ++ch) {
+                    const int h = h0 + (ch >> 1);
+                    const int sub = ch & 1;
                     uint8_t* xrow = xst + h * kBoxBytes + rr * 128;
-                    const uint8_t* arow = xst + kXTile + h * kBoxBytes + rr * 128;
-#pragma unroll
-                    for (int sub = 0; sub < 2; ++sub) {
-                        uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)ab * kStrip +
-                                                    (uint32_t)(h * 64 + sub * 32), v);
-                        ptx::tc_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int ch = sub * 4 + i;
-                            const uint32_t off = (uint32_t)((ch ^ (rr & 7)) << 4);
-                            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + off);
-                            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                            uint32_t o[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float x0 = __uint_as_float(xw[e] << 16);
-                                const float x1 = __uint_as_float(xw[e] & 0xFFFF0000u);
-                                const float d0 = fmaf(c, x0, __uint_as_float(v[i * 8 + 2 * e]));
-                                const float d1 = fmaf(c, x1, __uint_as_float(v[i * 8 + 2 * e + 1]));
-                                o[e] = pack_bf16x2(d0, d1);
-                            }
-                            if (ADD) {
-                                const uint4 av = *reinterpret_cast<const uint4*>(arow + off);
-                                const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float s0 = __uint_as_float(o[e] << 16) + __uint_as_float(aw[e] << 16);
-                                    const float s1 = __uint_as_float(o[e] & 0xFFFF0000u) +
-                                                     __uint_as_float(aw[e] & 0xFFFF0000u);
-                                    o[e] = pack_bf16x2(s0, s1);
-                                }
-                            }
-                            *reinterpret_cast<uint4*>(xrow + off) = make_uint4(o[0], o[1], o[2], o[3]);
-                        }
+                    const uint8_t* arow = xst + C::st_add + h * kBoxBytes + rr * 128;
+                    if (ch + 1 < 2 * C::HPW) {
+                        if (ch & 1) ptx::tmem_ld_32x32b_x32(tcol + (uint32_t)(ch + 1) * 32, va);
+                        else ptx::tmem_ld_32x32b_x32(tcol + (uint32_t)(ch + 1) * 32, vb);
                     }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && tok0 + q * 32 < p.T && I.col0 + h * kBoxCols < p.K)
-                        ptx::tma_store_2d(&dx_map, ptx::smem_u32(xst + h * kBoxBytes + q * 32 * 128),
-                                          I.col0 + h * kBoxCols, tok0 + q * 32, pol);
+                    if (ch & 1) epi_chunk<ADD>(vb, c, xrow, arow, rr, sub);
+                    else epi_chunk<ADD>(va, c, xrow, arow, rr, sub);
+                    if (ch + 1 < 2 * C::HPW) {
+                        if (ch & 1) ptx::tc_wait_ld_regs(va);
+                        else ptx::tc_wait_ld_regs(vb);
+                    }
+                    if (sub == 1) {
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && tok0 + q * 32 < p.T && I.col0 + h * kBoxCols < p.K)
+                            ptx::tma_store_2d(&maps.dx, ptx::smem_u32(xst + h * kBoxBytes + q * 32 * 128),
+                                              I.col0 + h * kBoxCols, tok0 + q * 32, pol);
+                    }
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -500,10 +551,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             uint32_t d0[16], d1[16], d2[16];
             const uint32_t dcol = tmem + lane_base + kDwCol + (uint32_t)db * kDwColStride;
-            ptx::tmem_ld_32x32b_x16(dcol, d0);
-            ptx::tmem_ld_32x32b_x16(dcol + 16, d1);
-            ptx::tmem_ld_32x32b_x16(dcol + 32, d2);
+            const bool lo_part = (C::HPW == 2) || h0 == 0;   // j 0..15
+            const bool hi_part = (C::HPW == 2) || h0 == 1;   // j 16..23
+            if (lo_part) {
+                ptx::tmem_ld_32x32b_x16(dcol, d0);
+                ptx::tmem_ld_32x32b_x16(dcol + 16, d1);
+            }
+            if (hi_part) ptx::tmem_ld_32x32b_x16(dcol + 32, d2);
             ptx::tc_wait_ld();
+            ptx::reg_fence16(d0);
+            ptx::reg_fence16(d1);
+            ptx::reg_fence16(d2);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(C::B_DE + db));
@@ -512,12 +570,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* dst = p.partial + (size_t)I.chunk * kNProj * p.K + col;
                 // accumulator columns: 0-15 X^T Ph[0..15], 16-31 X^T Pl[0..15],
                 //                      32-39 X^T Ph[16..23], 40-47 X^T Pl[16..23]
+                if (lo_part) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    dst[(size_t)j * p.K] = __uint_as_float(d0[j]) + __uint_as_float(d1[j]);
+                    for (int j = 0; j < 16; ++j)
+                        dst[(size_t)j * p.K] = __uint_as_float(d0[j]) + __uint_as_float(d1[j]);
+                }
+                if (hi_part) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[(size_t)(16 + i) * p.K] = __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]);
+                    for (int i = 0; i < 8; ++i)
+                        dst[(size_t)(16 + i) * p.K] = __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]);
+                }
             }
         }
         if (lane == 0) ptx::bulk_wait<0>();   // all dX stores of this warp are complete
@@ -532,29 +594,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-}  // namespace
-
-size_t smem_bytes(bool has_addend) {
-    return has_addend ? Cfg<true>::alloc : Cfg<false>::alloc;
+template <bool ADD, int NEPI>
+cudaError_t setup_one() {
+    return cudaFuncSetAttribute(main_tc_kernel<ADD, NEPI>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Cfg<ADD, NEPI>::alloc);
 }
 
-cudaError_t setup(bool has_addend) {
-    if (has_addend)
-        return cudaFuncSetAttribute(main_tc_kernel<true>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)Cfg<true>::alloc);
-    return cudaFuncSetAttribute(main_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Cfg<false>::alloc);
+template <bool ADD, int NEPI>
+cudaError_t launch_one(const MainParams& p, const Maps& m, int grid, cudaStream_t stream) {
+    main_tc_kernel<ADD, NEPI><<<grid, Cfg<ADD, NEPI>::threads, Cfg<ADD, NEPI>::alloc, stream>>>(p, m);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t smem_bytes(bool has_addend, int epi_warps) {
+    if (epi_warps == 4) return has_addend ? Cfg<true, 4>::alloc : Cfg<false, 4>::alloc;
+    return has_addend ? Cfg<true, 8>::alloc : Cfg<false, 8>::alloc;
+}
+
+cudaError_t setup(bool has_addend, int epi_warps) {
+    if (epi_warps == 4) return has_addend ? setup_one<true, 4>() : setup_one<false, 4>();
+    return has_addend ? setup_one<true, 8>() : setup_one<false, 8>();
 }
 
 cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensorMap& dx_map,
-                   const CUtensorMap& add_map, int grid, cudaStream_t stream) {
-    if (p.addend != nullptr)
-        main_tc_kernel<true><<<grid, kThreads, Cfg<true>::alloc, stream>>>(p, x_map, dx_map, add_map);
-    else
-        main_tc_kernel<false><<<grid, kThreads, Cfg<false>::alloc, stream>>>(p, x_map, dx_map,
-                                                                             add_map);
-    return cudaGetLastError();
+                   const CUtensorMap& add_map, const CUtensorMap& gp_map, const CUtensorMap& gr_map,
+                   const CUtensorMap& r_map, int grid, int epi_warps, cudaStream_t stream) {
+    Maps m;
+    m.x = x_map;
+    m.dx = dx_map;
+    m.add = add_map;
+    m.gp = gp_map;
+    m.gr = gr_map;
+    m.r = r_map;
+    const bool add = p.addend != nullptr;
+    if (epi_warps == 4) return add ? launch_one<true, 4>(p, m, grid, stream) : launch_one<false, 4>(p, m, grid, stream);
+    return add ? launch_one<true, 8>(p, m, grid, stream) : launch_one<false, 8>(p, m, grid, stream);
 }
 
 }  // namespace tc
