@@ -96,9 +96,12 @@ bool encode_f32_map(CUtensorMap* m, const void* base, int64_t T, int cols, uint3
     if (!enc) return false;
     const cuuint32_t estr[2] = {1, 1};
     if (cols == 0) {
-        const cuuint64_t dims[1] = {(cuuint64_t)T};
-        const cuuint32_t box[1] = {box_rows};
-        return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<void*>(base), dims, nullptr,
+        // a [T] vector as a 2-D {T, 1} tensor (one row; its row stride is never
+        // used but must be a multiple of 16 bytes)
+        const cuuint64_t dims[2] = {(cuuint64_t)T, 1};
+        const cuuint64_t strides[1] = {(cuuint64_t)((T * 4 + 15) / 16 * 16)};
+        const cuuint32_t box[2] = {box_rows, 1};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
@@ -108,6 +111,19 @@ bool encode_f32_map(CUtensorMap* m, const void* base, int64_t T, int cols, uint3
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Encodes the six tensor maps of one execute; on failure names the map.
+const char* encode_maps(CUtensorMap (&m)[6], int64_t T, int64_t K, const void* x, const void* dx,
+                        const void* add, const void* gp, const void* gr, const void* r) {
+    if (!encode_bf16_map(&m[0], x, T, K, tc::kTokenTile)) return "tensor map of x";
+    if (!encode_bf16_map(&m[1], dx, T, K, 32)) return "tensor map of dx";
+    if (!encode_bf16_map(&m[2], add, T, K, tc::kTokenTile)) return "tensor map of grad_x_addend";
+    if (!encode_f32_map(&m[3], gp, T, kGradProjCols, kNProj, tc::kTokenTile))
+        return "tensor map of grad_proj";
+    if (!encode_f32_map(&m[4], gr, T, 0, 0, tc::kTokenTile)) return "tensor map of grad_r";
+    if (!encode_f32_map(&m[5], r, T, 0, 0, tc::kTokenTile)) return "tensor map of r";
+    return nullptr;
 }
 
 struct Range {
@@ -181,6 +197,12 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
         if ((e = fma::setup()) != cudaSuccess) return cuda_fail(e, "setup (FMA kernel)");
     } else {
         if (!get_encode()) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
+        // the tensor maps depend on the pointers, but their shapes can be
+        // checked now (encoding only records the address)
+        CUtensorMap m[6];
+        const void* fake = reinterpret_cast<const void*>(uintptr_t(1) << 20);
+        if (const char* bad = encode_maps(m, T, K, fake, fake, fake, fake, fake, fake))
+            return cuda_fail(cudaErrorInvalidValue, bad);
     }
 
     mhcpb_plan_s* p = new mhcpb_plan_s();
@@ -301,14 +323,11 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float
         e = fma::launch(p, st);
         if (e != cudaSuccess) return cuda_fail(e, "launch (FMA kernel)");
     } else {
-        CUtensorMap xm, dxm, am, gpm, grm, rm;
-        if (!encode_bf16_map(&xm, x, T, K, tc::kTokenTile) || !encode_bf16_map(&dxm, dx, T, K, 32) ||
-            !encode_bf16_map(&am, add ? grad_x_addend : x, T, K, tc::kTokenTile) ||
-            !encode_f32_map(&gpm, grad_proj, T, kGradProjCols, kNProj, tc::kTokenTile) ||
-            !encode_f32_map(&grm, grad_r, T, 0, 0, tc::kTokenTile) ||
-            !encode_f32_map(&rm, r, T, 0, 0, tc::kTokenTile))
-            return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-        e = tc::launch(p, xm, dxm, am, gpm, grm, rm, plan->grid, plan->epi_warps, st);
+        CUtensorMap m[6];
+        if (const char* bad = encode_maps(m, T, K, x, dx, add ? grad_x_addend : x, grad_proj,
+                                          grad_r, r))
+            return cuda_fail(cudaErrorInvalidValue, bad);
+        e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], plan->grid, plan->epi_warps, st);
         if (e != cudaSuccess) return cuda_fail(e, "launch (tensor-core kernel)");
     }
     if (ev1 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev1), st)) != cudaSuccess)

@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     ptx::tma_load_2d(dst + kBoxBytes, &maps.x, I.col0 + kBoxCols, tok0, fb,
                                      pol_stream);
                     ptx::tma_load_2d(dst + C::st_p, &maps.gp, 0, tok0, fb, pol_keep);
-                    ptx::tma_load_1d(dst + C::st_gr, &maps.gr, tok0, fb, pol_keep);
-                    ptx::tma_load_1d(dst + C::st_r, &maps.r, tok0, fb, pol_keep);
+                    ptx::tma_load_2d(dst + C::st_gr, &maps.gr, tok0, 0, fb, pol_keep);
+                    ptx::tma_load_2d(dst + C::st_r, &maps.r, tok0, 0, fb, pol_keep);
                     if (ADD) {
                         ptx::tma_load_2d(dst + C::st_add, &maps.add, I.col0, tok0, fb, pol_stream);
                         ptx::tma_load_2d(dst + C::st_add + kBoxBytes, &maps.add,
