@@ -197,12 +197,6 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
         if ((e = fma::setup()) != cudaSuccess) return cuda_fail(e, "setup (FMA kernel)");
     } else {
         if (!get_encode()) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
-        // the tensor maps depend on the pointers, but their shapes can be
-        // checked now (encoding only records the address)
-        CUtensorMap m[6];
-        const void* fake = reinterpret_cast<const void*>(uintptr_t(1) << 20);
-        if (const char* bad = encode_maps(m, T, K, fake, fake, fake, fake, fake, fake))
-            return cuda_fail(cudaErrorInvalidValue, bad);
     }
 
     mhcpb_plan_s* p = new mhcpb_plan_s();
@@ -235,6 +229,18 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
         cudaFree(p->d_status);
         delete p;
         return cuda_fail(e, "cudaMemset (status word)");
+    }
+    if (!fma_kernel) {
+        // The tensor maps depend on the execute's pointers, but their shapes
+        // can be checked now: encode them over a real device address (the
+        // status word; encoding records the address and reads nothing).
+        CUtensorMap m[6];
+        const void* a = p->d_status;
+        if (const char* bad = encode_maps(m, T, K, a, a, a, a, a, a)) {
+            cudaFree(p->d_status);
+            delete p;
+            return cuda_fail(cudaErrorInvalidValue, bad);
+        }
     }
     *out = p;
     return MHCPB_OK;
