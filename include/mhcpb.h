@@ -70,7 +70,9 @@ typedef enum {
     MHCPB_ERR_WORKSPACE_TOO_SMALL = 7,
     MHCPB_ERR_CUDA = 8,               /* a CUDA runtime/driver call failed (see mhcpb_last_cuda_error) */
     MHCPB_ERR_DEVICE_TIMEOUT = 9,     /* reported by mhcpb_get_device_status */
-    MHCPB_ERR_UNSUPPORTED_DEVICE = 10 /* device is not compute capability 10.3 (GB300) */
+    MHCPB_ERR_UNSUPPORTED_DEVICE = 10, /* device is not compute capability 10.3 (GB300) */
+    MHCPB_ERR_SCRATCH_TOO_SMALL = 11  /* mhcpb_execute_static_scratch: the shape needs more
+                                         than MHCPB_STATIC_SCRATCH_BYTES of dW partials */
 } mhcpb_status_t;
 
 /* Plan flags. */
@@ -155,6 +157,45 @@ mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value);
  * with MHCPB_ERR_DEVICE_TIMEOUT in the status word.  Applies to executes
  * enqueued after the call. */
 mhcpb_status_t mhcpb_plan_set_wait_limit(mhcpb_plan_t plan, uint64_t nanoseconds);
+
+/* Size of the library's built-in scratch buffer (see below): 16 MiB. */
+#define MHCPB_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* The backward for callers that cannot allocate device memory at all: code
+ * running inside a host framework that owns every byte of the device heap
+ * (its own caching allocator, no cudaMalloc allowed), or plugin code that is
+ * handed its input and output buffers and nothing else.  Such a caller cannot
+ * create a plan (mhcpb_plan_create allocates the plan's status word) nor pass a
+ * workspace.  This entry point needs neither: it runs the same two kernels as
+ * mhcpb_execute (tensor-core streaming kernel, then the fixed-order reduction)
+ * with the dW partials kept in a buffer the library itself declares as a
+ * file-scope __device__ array of MHCPB_STATIC_SCRATCH_BYTES.  No counterpart
+ * on the pages: their API always takes a caller-allocated workspace.
+ *
+ *  - No cudaMalloc, cudaFree or other allocating call is made.  The buffer is
+ *    part of the loaded module: every GPU that loads the library holds its
+ *    16 MiB until the process exits.
+ *  - Shapes needing more than that are rejected with
+ *    MHCPB_ERR_SCRATCH_TOO_SMALL: S * 24 * K * 4 bytes with
+ *    S = ceil(T / MHCPB_TOKENS_PER_PARTIAL), i.e. up to T = 4096 at K = 20480.
+ *  - Runs on the calling thread's current device; all pointers must be device
+ *    memory there, 16-byte aligned and disjoint (same contract and status codes
+ *    as mhcpb_execute).  `flags` must contain MHCPB_ALLOW_TF32 and may contain
+ *    MHCPB_HAS_ADDEND (then `grad_x_addend` is required), nothing else.
+ *  - The first call on a device does that device's set-up (looks up the
+ *    buffer's device address, raises the kernels' shared-memory limit).  Make
+ *    that first call before any stream capture.
+ *  - Every call, on every stream, shares the one buffer and leaves the last
+ *    call's partials in it (nothing in it needs to start at zero: each execute
+ *    overwrites every partial it reads).  Calls that may overlap on the GPU
+ *    race on the buffer: order them on one stream or with events.
+ *  - A device-side wait timeout leaves the outputs undefined and is recorded
+ *    in a device word that this entry point does not report. */
+mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uint32_t flags,
+                                            const void* x, const float* w, const float* grad_proj,
+                                            const float* grad_r, const float* r,
+                                            void* dx, float* dw,
+                                            const void* grad_x_addend, void* stream);
 
 /* Releases the plan (and its status word).  Safe on NULL. */
 mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan);

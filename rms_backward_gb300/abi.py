@@ -24,6 +24,7 @@ MHCPB_ERR_WORKSPACE_TOO_SMALL = 7
 MHCPB_ERR_CUDA = 8
 MHCPB_ERR_DEVICE_TIMEOUT = 9
 MHCPB_ERR_UNSUPPORTED_DEVICE = 10
+MHCPB_ERR_SCRATCH_TOO_SMALL = 11
 
 MHCPB_ALLOW_TF32 = 1
 MHCPB_HAS_ADDEND = 2
@@ -33,12 +34,14 @@ MHCPB_TEST_INJECT_STALL = 1 << 30
 MHCPB_NPROJ = 24
 MHCPB_GRAD_PROJ_COLS = 32
 MHCPB_TOKENS_PER_PARTIAL = 512
+MHCPB_STATIC_SCRATCH_BYTES = 16 << 20
 
 QUERY = {"T": 0, "K": 1, "S": 2, "grid": 3, "flags": 4, "smem": 5, "token_tile": 6, "strip": 7}
 
 EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcpb_execute_profiled",
             "mhcpb_get_device_status", "mhcpb_plan_query", "mhcpb_plan_set_wait_limit",
-            "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error")
+            "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error",
+            "mhcpb_execute_static_scratch")
 
 
 class MhcpbError(RuntimeError):
@@ -71,6 +74,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_get_device_status.argtypes = [P, ctypes.POINTER(I32), I32]
     lib.mhcpb_plan_query.argtypes = [P, I32, ctypes.POINTER(I64)]
     lib.mhcpb_plan_set_wait_limit.argtypes = [P, ctypes.c_uint64]
+    lib.mhcpb_execute_static_scratch.argtypes = [I64, I64, U32, P, P, P, P, P, P, P, P, P]
     lib.mhcpb_destroy.argtypes = [P]
     lib.mhcpb_status_string.argtypes = [I32]
     lib.mhcpb_status_string.restype = ctypes.c_char_p
@@ -78,7 +82,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_last_cuda_error.restype = ctypes.c_char_p
     for name in ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute",
                  "mhcpb_execute_profiled", "mhcpb_get_device_status", "mhcpb_plan_query",
-                 "mhcpb_plan_set_wait_limit", "mhcpb_destroy"):
+                 "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -143,3 +147,13 @@ def mhcpb_status_string(status: int) -> str:
 
 def mhcpb_last_cuda_error() -> str:
     return load().mhcpb_last_cuda_error().decode()
+
+
+def mhcpb_execute_static_scratch(T: int, K: int, flags: int, x: int, w: int, grad_proj: int,
+                                 grad_r: int, r: int, dx: int, dw: int,
+                                 grad_x_addend: int | None, stream: int | None) -> None:
+    """The backward without plan or workspace: dW partials in the library's
+    built-in 16 MiB device buffer (for callers that cannot allocate)."""
+    _check(load().mhcpb_execute_static_scratch(int(T), int(K), int(flags), x, w, grad_proj, grad_r,
+                                               r, dx, dw, grad_x_addend or None, stream or None),
+           "mhcpb_execute_static_scratch")

@@ -145,6 +145,15 @@ mhcpb_status_t check_device_ptr(const void* ptr, int device) {
 
 }  // namespace
 
+namespace mhcpb {
+const char* encode_tc_maps(CUtensorMap (&m)[6], int64_t T, int64_t K, const void* x,
+                           const void* dx, const void* add, const void* gp, const void* gr,
+                           const void* r) {
+    return encode_maps(m, T, K, x, dx, add, gp, gr, r);
+}
+int record_cuda_error(cudaError_t e, const char* what) { return (int)cuda_fail(e, what); }
+}  // namespace mhcpb
+
 extern "C" {
 
 const char* mhcpb_status_string(mhcpb_status_t s) {
@@ -160,6 +169,8 @@ const char* mhcpb_status_string(mhcpb_status_t s) {
         case MHCPB_ERR_CUDA: return "CUDA error";
         case MHCPB_ERR_DEVICE_TIMEOUT: return "a wait inside the kernel timed out";
         case MHCPB_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3";
+        case MHCPB_ERR_SCRATCH_TOO_SMALL:
+            return "shape needs more dW-partial scratch than the built-in 16 MiB buffer";
     }
     return "unknown status";
 }

@@ -58,6 +58,15 @@ cudaError_t setup();
 cudaError_t launch(const MainParams& p, cudaStream_t stream);
 }  // namespace fma
 
+// Host helpers shared by the entry points (defined in mhcpb_api.cu).
+// encode_tc_maps: the six tensor maps of the tensor-core kernel; returns the
+// name of the map that failed, or null.  record_cuda_error: stores the
+// thread's CUDA error text and returns MHCPB_ERR_CUDA.
+const char* encode_tc_maps(CUtensorMap (&m)[6], int64_t T, int64_t K, const void* x,
+                           const void* dx, const void* add, const void* gp, const void* gr,
+                           const void* r);
+int record_cuda_error(cudaError_t e, const char* what);
+
 // Second kernel: dW[j,k] = sum over s ascending of partial[s][j][k].
 cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, cudaStream_t stream);
 
