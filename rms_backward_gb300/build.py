@@ -39,15 +39,22 @@ def _newest_header() -> float:
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def build(verbose: bool = False, extra_flags=None) -> str:
+def build(verbose: bool = False, extra_flags=None, out_dir=None) -> str:
+    """Compile and link; returns the library path.  ``extra_flags`` (extra nvcc
+    defines for instrumented copies) require ``out_dir`` so that the product
+    library in ``_build/`` is never replaced by an instrumented one."""
+    if extra_flags and not out_dir:
+        raise ValueError("extra_flags need a separate out_dir")
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    bdir = out_dir or BUILD
+    lib = os.path.join(bdir, "libmhcpb.so")
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_t = _newest_header()
     flags = NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), hdr_t) \
                 and not extra_flags:
             return obj, None
@@ -65,15 +72,15 @@ def build(verbose: bool = False, extra_flags=None) -> str:
     if errs:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errs))
     objs = [o for o, _ in results]
-    if not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + ".tmp"
+    if not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc, "-shared", "--cudart", "static", *ARCH, "-o", tmp, *objs,
                "-ldl", "-lrt", "-lpthread"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n$ {' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

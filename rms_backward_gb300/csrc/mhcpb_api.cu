@@ -29,6 +29,8 @@ struct mhcpb_plan_s {
     uint32_t* d_status = nullptr;
     uint64_t timeout_ns = 1000000000ull;  // 1 s bound on every in-kernel wait
     int epi_warps = 8;    // epilogue warps of the tensor-core kernel (4 or 8)
+    uint64_t* d_trace = nullptr;  // timeline stamps (builds with MHCPB_TRACE only)
+    size_t trace_bytes = 0;
 };
 
 namespace {
@@ -252,6 +254,14 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
             delete p;
             return cuda_fail(cudaErrorInvalidValue, bad);
         }
+#ifdef MHCPB_TRACE
+        p->trace_bytes = (size_t)p->grid * kTraceEvents * kTraceTiles * sizeof(uint64_t);
+        if (cudaMalloc(&p->d_trace, p->trace_bytes) != cudaSuccess ||
+            cudaMemset(p->d_trace, 0, p->trace_bytes) != cudaSuccess) {
+            delete p;
+            return cuda_fail(cudaErrorMemoryAllocation, "trace buffer");
+        }
+#endif
     }
     *out = p;
     return MHCPB_OK;
@@ -332,6 +342,7 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float
     p.status = plan->d_status;
     p.timeout_ns = plan->timeout_ns;
     p.test_flags = (plan->flags & MHCPB_TEST_INJECT_STALL) ? kTestInjectStall : 0u;
+    p.trace = plan->d_trace;
 
     cudaError_t e;
     if (ev0 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev0), st)) != cudaSuccess)
@@ -402,9 +413,20 @@ mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan) {
     if (plan->d_status) {
         DeviceGuard g(plan->device);
         cudaFree(plan->d_status);
+        if (plan->d_trace) cudaFree(plan->d_trace);
     }
     delete plan;
     return MHCPB_OK;
 }
+
+#ifdef MHCPB_TRACE
+// Instrumented builds only: copies the last execute's timeline stamps.
+mhcpb_status_t mhcpb_debug_trace(mhcpb_plan_t plan, void* host, size_t bytes) {
+    if (plan == nullptr || host == nullptr || bytes < plan->trace_bytes) return MHCPB_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    cudaError_t e = cudaMemcpy(host, plan->d_trace, plan->trace_bytes, cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? MHCPB_OK : cuda_fail(e, "cudaMemcpy (trace)");
+}
+#endif
 
 }  // extern "C"

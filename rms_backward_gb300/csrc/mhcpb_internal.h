@@ -31,7 +31,12 @@ struct MainParams {
     uint32_t* status;     // device status word
     uint64_t timeout_ns;  // bound on every wait inside the kernel
     uint32_t test_flags;  // kTestInjectStall: the MMA issuer waits on a barrier nothing completes
+    uint64_t* trace;      // timeline stamps, only in builds with MHCPB_TRACE (else null)
 };
+
+// Timeline stamps of a traced build: [grid][kTraceEvents][kTraceTiles] u64.
+constexpr int kTraceEvents = 12;
+constexpr int kTraceTiles = 48;
 
 constexpr uint32_t kTestInjectStall = 1u;
 

@@ -31,9 +31,9 @@
 //    write the result over the X tile in place and TMA-store it.  At the end
 //    of each chunk they write the chunk's dW partial (hi and lo halves summed)
 //    to the workspace.
-//  * Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2 operand
+//  * Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-3 operand
 //    preparation (TF32 rounding and BF16 hi/lo split of P and W into the
-//    tensor-core operand layout, from shared memory), 3 idle, 4.. epilogue.
+//    tensor-core operand layout, from shared memory), 4.. epilogue.
 //  * Every mbarrier wait is bounded (see wait_bar): on timeout the kernel
 //    records a status word, drains its own copies and MMAs and exits.
 #include <cuda_bf16.h>
@@ -107,6 +107,24 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile ui
         }
     }
 }
+
+// Timeline stamps for instrumented builds (MHCPB_TRACE); nothing otherwise.
+#ifdef MHCPB_TRACE
+#define TRACE(ev, n)                                                                        \
+    do {                                                                                    \
+        if (p.trace != nullptr && (n) < kTraceTiles)                                       \
+            p.trace[((size_t)blockIdx.x * kTraceEvents + (ev)) * kTraceTiles + (n)] =      \
+                ptx::globaltimer();                                                         \
+    } while (0)
+#else
+#define TRACE(ev, n) \
+    do {             \
+    } while (0)
+#endif
+enum TraceEvent {
+    EV_PROD_ISSUE = 0, EV_MMA_XFULL, EV_MMA_PFULL, EV_MMA_ACCEMPTY, EV_MMA_ISSUED, EV_EPI_ACCFULL,
+    EV_EPI_STORED, EV_EPI_RELEASE, EV_PREP_XFULL, EV_PREP_PEMPTY, EV_PREP_DONE, EV_PROD_XEMPTY
+};
 
 __device__ __forceinline__ float tf32_rna(float v) {
     uint32_t u;
@@ -234,7 +252,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             ptx::mbar_init(bar(C::B_XE + s), NEPI);
         }
         for (int s = 0; s < NP; ++s) {
-            ptx::mbar_init(bar(C::B_PF + s), 1);
+            ptx::mbar_init(bar(C::B_PF + s), 2);
             ptx::mbar_init(bar(C::B_PE + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -243,7 +261,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             ptx::mbar_init(bar(C::B_DF + b), 1);
             ptx::mbar_init(bar(C::B_DE + b), NEPI);
         }
-        ptx::mbar_init(bar(C::B_WF), 1);
+        ptx::mbar_init(bar(C::B_WF), 2);
         ptx::mbar_init(bar(C::B_WE), 1);
         ptx::mbar_init(bar(C::B_FIN), 1);
         *abort_flag = 0u;
@@ -278,13 +296,15 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             uint32_t ph = 0;
             uint32_t issued = 0, last_par = 0;
             bool ok = true;
+            int n = 0;   // tile counter of this CTA (trace index)
             for (int it = it_begin; it < it_end && ok; ++it) {
                 const Item I = item_at(p, it);
-                for (int tt = 0; tt < I.ntiles; ++tt) {
+                for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
                     if (!wait_bar(bar(C::B_XE + st), ph ^ 1u, abort_flag, p.status, tmo, true)) {
                         ok = false;
                         break;
                     }
+                    TRACE(EV_PROD_XEMPTY, n);
                     const int tok0 = I.t_begin + tt * kTokenTile;
                     const uint32_t dst = sbase + (uint32_t)st * C::stage_bytes;
                     const uint32_t fb = bar(C::B_XF + st);
@@ -300,6 +320,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                         ptx::tma_load_2d(dst + C::st_add + kBoxBytes, &maps.add,
                                          I.col0 + kBoxCols, tok0, fb, pol_stream);
                     }
+                    TRACE(EV_PROD_ISSUE, n);
                     issued |= 1u << st;
                     last_par = (last_par & ~(1u << st)) | (ph << st);
                     if (++st == NS) {
@@ -325,7 +346,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             const uint32_t w_base = sbase + C::off_w;
             int xs = 0, ps = 0, ab = 0;
             uint32_t xph = 0, pph = 0, aph = 0;
-            int n_w = 0, prev_strip = -1, local = 0;
+            int n_w = 0, prev_strip = -1, local = 0, n = 0;
             bool ok = true;
             // failure-detection test hook: nothing arrives on the final barrier
             // before the drain below, so this wait can only run out of time
@@ -348,13 +369,22 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     break;
                 }
                 const uint32_t d_dw = tmem + kDwCol + (uint32_t)db * kDwColStride;
-                for (int tt = 0; tt < I.ntiles; ++tt) {
-                    if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true) ||
-                        !wait_bar(bar(C::B_PF + ps), pph, abort_flag, p.status, tmo, true) ||
-                        !wait_bar(bar(C::B_AE + ab), aph ^ 1u, abort_flag, p.status, tmo, true)) {
+                for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
+                    if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
                         ok = false;
                         break;
                     }
+                    TRACE(EV_MMA_XFULL, n);
+                    if (!wait_bar(bar(C::B_PF + ps), pph, abort_flag, p.status, tmo, true)) {
+                        ok = false;
+                        break;
+                    }
+                    TRACE(EV_MMA_PFULL, n);
+                    if (!wait_bar(bar(C::B_AE + ab), aph ^ 1u, abort_flag, p.status, tmo, true)) {
+                        ok = false;
+                        break;
+                    }
+                    TRACE(EV_MMA_ACCEMPTY, n);
                     ptx::tc_fence_after();
                     const uint32_t pA = sbase + C::off_p + (uint32_t)ps * kPStage;
                     const uint32_t xA = sbase + (uint32_t)xs * C::stage_bytes;
@@ -379,6 +409,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     }
                     ptx::tc_commit(bar(C::B_PE + ps));
                     ptx::tc_commit(bar(C::B_AF + ab));
+                    TRACE(EV_MMA_ISSUED, n);
                     if (++xs == NS) { xs = 0; xph ^= 1u; }
                     if (++ps == NP) { ps = 0; pph ^= 1u; }
                     if (++ab == 2) { ab = 0; aph ^= 1u; }
@@ -394,9 +425,12 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             wait_bar(bar(C::B_FIN), 0u, abort_flag, p.status, tmo, false);
         }
         __syncwarp();
-    } else if (warp == 2) {
+    } else if (warp == 2 || warp == 3) {
         // ------------------------------------------------------------ operand preparation
-        int xs = 0, ps = 0;
+        // two warps: each converts half of the strip's W columns and half of
+        // every tile's tokens; P_FULL and W_FULL complete when both arrived
+        const int pw = warp - 2;
+        int xs = 0, ps = 0, n = 0;
         uint32_t xph = 0, pph = 0;
         int n_w = 0, prev_strip = -1;
         bool ok = true;
@@ -404,10 +438,10 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             const Item I = item_at(p, it);
             if (I.strip != prev_strip) {
                 // W columns of this lane, fetched before waiting for the buffer
-                float wv[4][kNProj];
+                float wv[2][kNProj];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int col = I.col0 + lane + 32 * q;
+                for (int q = 0; q < 2; ++q) {
+                    const int col = I.col0 + pw * 64 + lane + 32 * q;
 #pragma unroll
                     for (int j = 0; j < kNProj; ++j)
                         wv[q][j] = col < p.K ? __ldg(p.w + (size_t)j * p.K + col) : 0.f;
@@ -419,8 +453,8 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 }
                 uint8_t* wsm = smem + C::off_w;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int cc = lane + 32 * q;
+                for (int q = 0; q < 2; ++q) {
+                    const int cc = pw * 64 + lane + 32 * q;
                     uint16_t hi[kNProj], lo[kNProj];
 #pragma unroll
                     for (int j = 0; j < kNProj; ++j) split_tf32(tf32_rna(wv[q][j]), hi[j], lo[j]);
@@ -435,17 +469,22 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 ++n_w;
                 prev_strip = I.strip;
             }
-            for (int tt = 0; tt < I.ntiles; ++tt) {
-                if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true) ||
-                    !wait_bar(bar(C::B_PE + ps), pph ^ 1u, abort_flag, p.status, tmo, true)) {
+            for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
+                if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
                     ok = false;
                     break;
                 }
+                if (pw == 0) TRACE(EV_PREP_XFULL, n);
+                if (!wait_bar(bar(C::B_PE + ps), pph ^ 1u, abort_flag, p.status, tmo, true)) {
+                    ok = false;
+                    break;
+                }
+                if (pw == 0) TRACE(EV_PREP_PEMPTY, n);
                 const float* praw = reinterpret_cast<const float*>(smem + (uint32_t)xs * C::stage_bytes + C::st_p);
                 uint8_t* psm = smem + C::off_p + ps * kPStage;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tok = lane + 32 * i;   // rows past T arrive as zeros (TMA fill)
+                for (int i = 0; i < 2; ++i) {
+                    const int tok = pw * 64 + lane + 32 * i;   // rows past T arrive as zeros (TMA fill)
                     float f[kNProj];
 #pragma unroll
                     for (int q = 0; q < 6; ++q) {
@@ -463,6 +502,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(C::B_PF + ps));
+                if (pw == 0) TRACE(EV_PREP_DONE, n);
                 if (++xs == NS) { xs = 0; xph ^= 1u; }
                 if (++ps == NP) { ps = 0; pph ^= 1u; }
             }
@@ -479,13 +519,13 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         const uint64_t pol = ptx::policy_evict_first();
         int xs = 0, ab = 0, local = 0;
         uint32_t xph = 0, aph = 0;
-        int pend = -1;                           // stage whose dX stores may still read smem
+        int pend = -1, n = 0;                    // stage whose dX stores may still read smem; tile counter
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it, ++local) {
             const Item I = item_at(p, it);
             const int db = local & 1;
             const uint32_t dph = (uint32_t)(local >> 1) & 1u;
-            for (int tt = 0; tt < I.ntiles; ++tt) {
+            for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
                 const int tok0 = I.t_begin + tt * kTokenTile;
                 if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
                     ok = false;
@@ -499,24 +539,32 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     ok = false;
                     break;
                 }
+                if (e == 0 && lane == 0) TRACE(EV_EPI_ACCFULL, n);
                 ptx::tc_fence_after();
                 const uint32_t tcol = tmem + lane_base + (uint32_t)ab * kStrip + (uint32_t)(h0 * 64);
                 uint32_t va[32], vb[32];
                 ptx::tmem_ld_32x32b_x32(tcol, va);
                 ptx::tc_wait_ld_regs(va);
+                constexpr int nch = 2 * C::HPW;   // 32-column chunks of this warp
 #pragma unroll
-                for (int ch = 0; ch < 2 * C::HPW; ++ch) {
+                for (int ch = 0; ch < nch; ++ch) {
                     const int h = h0 + (ch >> 1);
                     const int sub = ch & 1;
                     uint8_t* xrow = xst + h * kBoxBytes + rr * 128;
                     const uint8_t* arow = xst + C::st_add + h * kBoxBytes + rr * 128;
-                    if (ch + 1 < 2 * C::HPW) {
+                    if (ch + 1 < nch) {
                         if (ch & 1) ptx::tmem_ld_32x32b_x32(tcol + (uint32_t)(ch + 1) * 32, va);
                         else ptx::tmem_ld_32x32b_x32(tcol + (uint32_t)(ch + 1) * 32, vb);
+                    } else {
+                        // every accumulator column of this warp is in registers:
+                        // hand the TMEM buffer back to the MMA issuer
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(bar(C::B_AE + ab));
                     }
                     if (ch & 1) epi_chunk<ADD>(vb, c, xrow, arow, rr, sub);
                     else epi_chunk<ADD>(va, c, xrow, arow, rr, sub);
-                    if (ch + 1 < 2 * C::HPW) {
+                    if (ch + 1 < nch) {
                         if (ch & 1) ptx::tc_wait_ld_regs(va);
                         else ptx::tc_wait_ld_regs(vb);
                     }
@@ -528,16 +576,21 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                                               I.col0 + h * kBoxCols, tok0 + q * 32, pol);
                     }
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
                 if (lane == 0) {
-                    ptx::mbar_arrive(bar(C::B_AE + ab));
                     ptx::bulk_commit();
+                    if (e == 0) TRACE(EV_EPI_STORED, n);
+#ifdef MHCPB_DEFER_RELEASE
                     if (pend >= 0) {
                         ptx::bulk_wait_read<1>();      // the previous tile's stores have read smem
                         ptx::mbar_arrive(bar(C::B_XE + pend));
                     }
+#else
+                    ptx::bulk_wait_read<0>();          // this tile's stores have read smem
+                    ptx::mbar_arrive(bar(C::B_XE + xs));
+#endif
+                    if (e == 0) TRACE(EV_EPI_RELEASE, n);
                 }
+                __syncwarp();
                 pend = xs;
                 if (++xs == NS) { xs = 0; xph ^= 1u; }
                 if (++ab == 2) { ab = 0; aph ^= 1u; }
