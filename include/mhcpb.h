@@ -158,6 +158,13 @@ mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value);
  * enqueued after the call. */
 mhcpb_status_t mhcpb_plan_set_wait_limit(mhcpb_plan_t plan, uint64_t nanoseconds);
 
+/* Caps the tensor-core kernel's persistent grid at `max_ctas` CTAs (one per
+ * SM; 0 restores the default of every SM), e.g. to leave SMs to kernels that
+ * run concurrently on other streams.  Results are bitwise identical for every
+ * cap: the dW partition depends only on T.  No effect on MHCPB_FMA_KERNEL
+ * plans.  Applies to executes enqueued after the call. */
+mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas);
+
 /* Size of the library's built-in scratch buffer (see below): 16 MiB. */
 #define MHCPB_STATIC_SCRATCH_BYTES (16u << 20)
 

@@ -16,7 +16,8 @@ from . import abi
 from .abi import (  # noqa: F401
     MHCPB_ALLOW_TF32, MHCPB_FMA_KERNEL, MHCPB_HAS_ADDEND, MhcpbError, mhcpb_destroy,
     mhcpb_execute, mhcpb_get_device_status, mhcpb_last_cuda_error, mhcpb_plan_create,
-    mhcpb_plan_query, mhcpb_plan_set_wait_limit, mhcpb_status_string, mhcpb_workspace_bytes,
+    mhcpb_plan_query, mhcpb_plan_set_max_ctas, mhcpb_plan_set_wait_limit, mhcpb_status_string,
+    mhcpb_workspace_bytes,
 )
 
 
@@ -38,6 +39,9 @@ class Plan:
 
     def set_wait_limit(self, nanoseconds: int) -> None:
         mhcpb_plan_set_wait_limit(self.handle, nanoseconds)
+
+    def set_max_ctas(self, max_ctas: int) -> None:
+        mhcpb_plan_set_max_ctas(self.handle, max_ctas)
 
     def query(self, which: str) -> int:
         return mhcpb_plan_query(self.handle, which)

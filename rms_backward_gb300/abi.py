@@ -41,7 +41,7 @@ QUERY = {"T": 0, "K": 1, "S": 2, "grid": 3, "flags": 4, "smem": 5, "token_tile":
 EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcpb_execute_profiled",
             "mhcpb_get_device_status", "mhcpb_plan_query", "mhcpb_plan_set_wait_limit",
             "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error",
-            "mhcpb_execute_static_scratch")
+            "mhcpb_execute_static_scratch", "mhcpb_plan_set_max_ctas")
 
 
 class MhcpbError(RuntimeError):
@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_get_device_status.argtypes = [P, ctypes.POINTER(I32), I32]
     lib.mhcpb_plan_query.argtypes = [P, I32, ctypes.POINTER(I64)]
     lib.mhcpb_plan_set_wait_limit.argtypes = [P, ctypes.c_uint64]
+    lib.mhcpb_plan_set_max_ctas.argtypes = [P, I32]
     lib.mhcpb_execute_static_scratch.argtypes = [I64, I64, U32, P, P, P, P, P, P, P, P, P]
     lib.mhcpb_destroy.argtypes = [P]
     lib.mhcpb_status_string.argtypes = [I32]
@@ -82,7 +83,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_last_cuda_error.restype = ctypes.c_char_p
     for name in ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute",
                  "mhcpb_execute_profiled", "mhcpb_get_device_status", "mhcpb_plan_query",
-                 "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch"):
+                 "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch",
+                 "mhcpb_plan_set_max_ctas"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -135,6 +137,10 @@ def mhcpb_plan_query(plan: int, which) -> int:
 
 def mhcpb_plan_set_wait_limit(plan: int, nanoseconds: int) -> None:
     _check(load().mhcpb_plan_set_wait_limit(plan, int(nanoseconds)), "mhcpb_plan_set_wait_limit")
+
+
+def mhcpb_plan_set_max_ctas(plan: int, max_ctas: int) -> None:
+    _check(load().mhcpb_plan_set_max_ctas(plan, int(max_ctas)), "mhcpb_plan_set_max_ctas")
 
 
 def mhcpb_destroy(plan: int) -> None:

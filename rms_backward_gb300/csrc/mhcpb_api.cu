@@ -29,6 +29,7 @@ struct mhcpb_plan_s {
     uint32_t* d_status = nullptr;
     uint64_t timeout_ns = 1000000000ull;  // 1 s bound on every in-kernel wait
     int epi_warps = 8;    // epilogue warps of the tensor-core kernel (4 or 8)
+    int max_grid = 0;     // default grid of the tensor-core kernel (before any cap)
     uint64_t* d_trace = nullptr;  // timeline stamps (builds with MHCPB_TRACE only)
     size_t trace_bytes = 0;
 };
@@ -226,7 +227,8 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
     } else {
         p->n_strips = (int)((K + tc::kStrip - 1) / tc::kStrip);
         const int64_t items = (int64_t)p->n_strips * p->S;
-        p->grid = (int)(items < sms ? items : sms);
+        p->grid = tc::grid_size(items, sms);
+        p->max_grid = p->grid;
         if (const char* ev = std::getenv("MHCPB_EPI_WARPS")) p->epi_warps = std::atoi(ev) == 4 ? 4 : 8;
         if ((e = tc::setup(add, p->epi_warps)) != cudaSuccess) {
             delete p;
@@ -398,6 +400,13 @@ mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     }
     *status = static_cast<mhcpb_status_t>(v);
+    return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas) {
+    if (plan == nullptr || max_ctas < 0) return MHCPB_ERR_INVALID_ARG;
+    if (plan->flags & MHCPB_FMA_KERNEL) return MHCPB_OK;
+    plan->grid = (max_ctas == 0 || max_ctas > plan->max_grid) ? plan->max_grid : max_ctas;
     return MHCPB_OK;
 }
 

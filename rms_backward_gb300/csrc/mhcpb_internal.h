@@ -45,6 +45,12 @@ namespace tc {
 constexpr int kTokenTile = 128;    // MMA M for dX; K-extent of one dW MMA group
 constexpr int kStrip = 128;        // columns per strip: MMA N for dX, M for dW
 constexpr int kBoxCols = 64;       // TMA box width (128 bytes of BF16)
+// Persistent grid: one CTA per SM, at most one per schedule unit (half of a
+// (strip, chunk) item), so every CTA has work.
+inline int grid_size(int64_t items, int sms) {
+    const int64_t units = 2 * items;
+    return (int)(units < sms ? units : sms);
+}
 size_t smem_bytes(bool has_addend, int epi_warps);
 cudaError_t setup(bool has_addend, int epi_warps);
 // Tensor maps: x/dx/addend BF16 [T,K] boxes 64 x {128,32,128} (128-byte swizzle),

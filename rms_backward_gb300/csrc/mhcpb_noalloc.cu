@@ -142,7 +142,7 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
     if (const char* bad = encode_tc_maps(m, T, K, x, dx, add ? grad_x_addend : x, grad_proj, grad_r, r))
         return (mhcpb_status_t)record_cuda_error(cudaErrorInvalidValue, bad);
     const int64_t items = (int64_t)p.n_strips * p.S;
-    const int grid = (int)(items < s.sms ? items : s.sms);
+    const int grid = tc::grid_size(items, s.sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], grid, kEpiWarps, st)) != cudaSuccess)
         return (mhcpb_status_t)record_cuda_error(e, "launch (tensor-core kernel)");

@@ -156,11 +156,17 @@ __device__ __forceinline__ uint4 pack8(const uint16_t* s) {
     return v;
 }
 
-// Work-item geometry shared by all roles.
+// Work-item geometry shared by all roles.  The schedule unit is half an item
+// (64 of the strip's 128 columns): a CTA owns the contiguous unit range
+// [u_begin, u_end), so its first and last item may be half items (hmask 1 or
+// 2).  Splitting an item by columns leaves every dW partial's bits unchanged:
+// a column's partial depends only on that column's tokens, summed in the same
+// tile order whichever CTA computes it.
 struct Item {
     int strip, chunk, col0, t_begin, ntiles;
+    uint32_t hmask;   // bit h set: 64-column half h of the strip belongs to this CTA
 };
-__device__ __forceinline__ Item item_at(const MainParams& p, int it) {
+__device__ __forceinline__ Item item_at(const MainParams& p, int it, int u_begin, int u_end) {
     Item r;
     r.strip = it / p.S;
     r.chunk = it - r.strip * p.S;
@@ -168,6 +174,7 @@ __device__ __forceinline__ Item item_at(const MainParams& p, int it) {
     r.t_begin = r.chunk * kChunk;
     const int t_end = min(p.T, r.t_begin + kChunk);
     r.ntiles = (t_end - r.t_begin + kTokenTile - 1) / kTokenTile;
+    r.hmask = (2 * it >= u_begin ? 1u : 0u) | (2 * it + 1 < u_end ? 2u : 0u);
     return r;
 }
 
@@ -243,8 +250,11 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
     auto bar = [&](int i) -> uint32_t { return sbase + C::off_bar + 8u * (uint32_t)i; };
 
     const int n_items = p.n_strips * p.S;
-    const int it_begin = (int)((int64_t)blockIdx.x * n_items / gridDim.x);
-    const int it_end = (int)((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
+    const int n_units = 2 * n_items;             // gridDim.x <= n_units (host)
+    const int u_begin = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+    const int u_end = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+    const int it_begin = u_begin >> 1;
+    const int it_end = ((u_end - 1) >> 1) + 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             bool ok = true;
             int n = 0;   // tile counter of this CTA (trace index)
             for (int it = it_begin; it < it_end && ok; ++it) {
-                const Item I = item_at(p, it);
+                const Item I = item_at(p, it, u_begin, u_end);
                 for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
                     if (!wait_bar(bar(C::B_XE + st), ph ^ 1u, abort_flag, p.status, tmo, true)) {
                         ok = false;
@@ -308,17 +318,26 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     const int tok0 = I.t_begin + tt * kTokenTile;
                     const uint32_t dst = sbase + (uint32_t)st * C::stage_bytes;
                     const uint32_t fb = bar(C::B_XF + st);
-                    ptx::mbar_arrive_expect_tx(fb, C::stage_bytes);
-                    ptx::tma_load_2d(dst, &maps.x, I.col0, tok0, fb, pol_stream);
-                    ptx::tma_load_2d(dst + kBoxBytes, &maps.x, I.col0 + kBoxCols, tok0, fb,
-                                     pol_stream);
+                    // only this CTA's 64-column halves of X (and of the addend) are
+                    // fetched; the tensor cores still read the whole stage, and the
+                    // accumulator rows/columns of a missing half are never used
+                    const uint32_t nbox = (I.hmask & 1u) + (I.hmask >> 1);
+                    ptx::mbar_arrive_expect_tx(
+                        fb, C::stage_bytes - (2u - nbox) * kBoxBytes * (ADD ? 2u : 1u));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (I.hmask & (1u << h))
+                            ptx::tma_load_2d(dst + h * kBoxBytes, &maps.x, I.col0 + h * kBoxCols,
+                                             tok0, fb, pol_stream);
                     ptx::tma_load_2d(dst + C::st_p, &maps.gp, 0, tok0, fb, pol_keep);
                     ptx::tma_load_2d(dst + C::st_gr, &maps.gr, tok0, 0, fb, pol_keep);
                     ptx::tma_load_2d(dst + C::st_r, &maps.r, tok0, 0, fb, pol_keep);
                     if (ADD) {
-                        ptx::tma_load_2d(dst + C::st_add, &maps.add, I.col0, tok0, fb, pol_stream);
-                        ptx::tma_load_2d(dst + C::st_add + kBoxBytes, &maps.add,
-                                         I.col0 + kBoxCols, tok0, fb, pol_stream);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (I.hmask & (1u << h))
+                                ptx::tma_load_2d(dst + C::st_add + h * kBoxBytes, &maps.add,
+                                                 I.col0 + h * kBoxCols, tok0, fb, pol_stream);
                     }
                     TRACE(EV_PROD_ISSUE, n);
                     issued |= 1u << st;
@@ -353,7 +372,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             if (p.test_flags & kTestInjectStall)
                 ok = wait_bar(bar(C::B_FIN), 0u, abort_flag, p.status, tmo, true);
             for (int it = it_begin; it < it_end && ok; ++it, ++local) {
-                const Item I = item_at(p, it);
+                const Item I = item_at(p, it, u_begin, u_end);
                 const int db = local & 1;
                 const uint32_t dph = (uint32_t)(local >> 1) & 1u;
                 if (I.strip != prev_strip) {
@@ -435,7 +454,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         int n_w = 0, prev_strip = -1;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item I = item_at(p, it);
+            const Item I = item_at(p, it, u_begin, u_end);
             if (I.strip != prev_strip) {
                 // W columns of this lane, fetched before waiting for the buffer
                 float wv[2][kNProj];
@@ -522,7 +541,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         int pend = -1, n = 0;                    // stage whose dX stores may still read smem; tile counter
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it, ++local) {
-            const Item I = item_at(p, it);
+            const Item I = item_at(p, it, u_begin, u_end);
             const int db = local & 1;
             const uint32_t dph = (uint32_t)(local >> 1) & 1u;
             for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
@@ -540,6 +559,20 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     break;
                 }
                 if (e == 0 && lane == 0) TRACE(EV_EPI_ACCFULL, n);
+                const bool mine = (C::HPW == 2) ? (I.hmask != 0u) : (((I.hmask >> h0) & 1u) != 0u);
+                if (!mine) {
+                    // none of this warp's columns belong to this CTA in this item:
+                    // only hand the accumulator and the stage back
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::mbar_arrive(bar(C::B_AE + ab));
+                        ptx::mbar_arrive(bar(C::B_XE + xs));
+                    }
+                    __syncwarp();
+                    if (++xs == NS) { xs = 0; xph ^= 1u; }
+                    if (++ab == 2) { ab = 0; aph ^= 1u; }
+                    continue;
+                }
                 ptx::tc_fence_after();
                 const uint32_t tcol = tmem + lane_base + (uint32_t)ab * kStrip + (uint32_t)(h0 * 64);
                 uint32_t va[32], vb[32];
@@ -562,8 +595,11 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                         __syncwarp();
                         if (lane == 0) ptx::mbar_arrive(bar(C::B_AE + ab));
                     }
-                    if (ch & 1) epi_chunk<ADD>(vb, c, xrow, arow, rr, sub);
-                    else epi_chunk<ADD>(va, c, xrow, arow, rr, sub);
+                    const bool hv = ((I.hmask >> h) & 1u) != 0u;   // this half is the CTA's
+                    if (hv) {
+                        if (ch & 1) epi_chunk<ADD>(vb, c, xrow, arow, rr, sub);
+                        else epi_chunk<ADD>(va, c, xrow, arow, rr, sub);
+                    }
                     if (ch + 1 < nch) {
                         if (ch & 1) ptx::tc_wait_ld_regs(va);
                         else ptx::tc_wait_ld_regs(vb);
@@ -571,7 +607,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     if (sub == 1) {
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0 && tok0 + q * 32 < p.T && I.col0 + h * kBoxCols < p.K)
+                        if (lane == 0 && hv && tok0 + q * 32 < p.T && I.col0 + h * kBoxCols < p.K)
                             ptx::tma_store_2d(&maps.dx, ptx::smem_u32(xst + h * kBoxBytes + q * 32 * 128),
                                               I.col0 + h * kBoxCols, tok0 + q * 32, pol);
                     }
@@ -604,8 +640,10 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             ptx::tc_fence_after();
             uint32_t d0[16], d1[16], d2[16];
             const uint32_t dcol = tmem + lane_base + kDwCol + (uint32_t)db * kDwColStride;
-            const bool lo_part = (C::HPW == 2) || h0 == 0;   // j 0..15
-            const bool hi_part = (C::HPW == 2) || h0 == 1;   // j 16..23
+            // this warp's lanes are strip columns 32q..32q+31, i.e. half q / 2
+            const bool cols_mine = ((I.hmask >> (q >> 1)) & 1u) != 0u;
+            const bool lo_part = cols_mine && ((C::HPW == 2) || h0 == 0);   // j 0..15
+            const bool hi_part = cols_mine && ((C::HPW == 2) || h0 == 1);   // j 16..23
             if (lo_part) {
                 ptx::tmem_ld_32x32b_x16(dcol, d0);
                 ptx::tmem_ld_32x32b_x16(dcol + 16, d1);

@@ -93,7 +93,7 @@ def test_plan_facts():
     assert plan.workspace_bytes == 15_728_640
     assert plan.query("S") == 8
     assert plan.query("grid") == min(torch.cuda.get_device_properties(0).multi_processor_count,
-                                     160 * 8)
+                                     2 * 160 * 8)
     assert plan.query("smem") <= 232448
     plan.close()
 

@@ -97,3 +97,28 @@ def test_independent_plans_same_shape_agree():
     assert np.array_equal(da, db) and np.array_equal(wa, wb)
     a.plan.close()
     b.plan.close()
+
+
+@pytest.mark.parametrize("T,K", [(2000, 4096), (4096, 20480)])
+def test_bitwise_independent_of_grid_size(T, K):
+    """The dW partition depends only on T: capping the persistent grid at any
+    number of CTAs (which moves where items are split between CTAs) leaves dX
+    and dW bitwise unchanged, so results do not depend on the SM count."""
+    wl = WL.make("grid", T=T, K=K, seed=34)
+    r = Runner(wl)
+    full = r.plan.query("grid")
+    r.run()
+    dx0, dw0 = _bits(r)
+    caps = [full - 1, 100, 77, 37, 5] + ([1] if T * K <= 2000 * 4096 else [])
+    for cap in caps:
+        r.plan.set_max_ctas(cap)
+        assert r.plan.query("grid") == min(cap, full)
+        r.dx.fill_(0)
+        r.dw.fill_(float("nan"))
+        r.run()
+        dx, dw = _bits(r)
+        assert np.array_equal(dw, dw0), f"dW changed with {cap} CTAs"
+        assert np.array_equal(dx, dx0), f"dX changed with {cap} CTAs"
+    r.plan.set_max_ctas(0)
+    assert r.plan.query("grid") == full
+    r.plan.close()
