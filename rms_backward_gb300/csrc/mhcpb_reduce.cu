@@ -9,7 +9,9 @@
 // One thread owns four consecutive dW elements; the sum runs over s in
 // ascending order, so dW depends only on (T, K) and the inputs.  Launched as a
 // programmatic dependent of the streaming kernel: it may be scheduled while
-// that kernel drains and waits for its completion before reading.
+// that kernel drains and waits for its completion before reading.  The
+// partials are dead once read: with a 128-byte-aligned workspace their L2
+// lines are dropped without being written back to HBM.
 #include "mhcpb_internal.h"
 #include "ptx.cuh"
 
@@ -18,37 +20,47 @@ namespace mhcpb {
 namespace {
 
 constexpr int kReduceThreads = 256;
+constexpr int kGroup = 8;   // partials loaded before they are summed
 
 __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4* __restrict__ part,
                                                                    float4* __restrict__ dw, int S,
-                                                                   int64_t n4) {
+                                                                   int64_t n4, int discard) {
     ptx::grid_dependency_wait();
     const int64_t i = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x;
-    if (i >= n4) return;
-    float4 a = part[i];
-    int s = 1;
-    // loads of a group are independent; the additions keep ascending s
-    for (; s + 4 <= S; s += 4) {
-        const float4 b0 = part[(int64_t)(s + 0) * n4 + i];
-        const float4 b1 = part[(int64_t)(s + 1) * n4 + i];
-        const float4 b2 = part[(int64_t)(s + 2) * n4 + i];
-        const float4 b3 = part[(int64_t)(s + 3) * n4 + i];
-        a.x += b0.x; a.y += b0.y; a.z += b0.z; a.w += b0.w;
-        a.x += b1.x; a.y += b1.y; a.z += b1.z; a.w += b1.w;
-        a.x += b2.x; a.y += b2.y; a.z += b2.z; a.w += b2.w;
-        a.x += b3.x; a.y += b3.y; a.z += b3.z; a.w += b3.w;
+    const bool valid = i < n4;   // n4 % 8 == 0: a 128-byte line is all valid or all not
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; valid && s0 < S; s0 += kGroup) {
+        float4 b[kGroup];
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g)
+            if (s0 + g < S) b[g] = part[(int64_t)(s0 + g) * n4 + i];
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+            if (s0 + g < S) {
+                if (s0 + g == 0) {
+                    a = b[g];
+                } else {
+                    a.x += b[g].x; a.y += b[g].y; a.z += b[g].z; a.w += b[g].w;
+                }
+            }
+        }
     }
-    for (; s < S; ++s) {
-        const float4 b = part[(int64_t)s * n4 + i];
-        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    if (valid) dw[i] = a;
+    // Every lane of a 128-byte line (8 float4) has consumed its loads once the
+    // warp has converged here; then one lane per line drops the line.
+    __syncwarp();
+    if (valid && discard && (i & 7) == 0) {
+        for (int s = 0; s < S; ++s) ptx::discard_l2_line(part + (int64_t)s * n4 + i);
     }
-    dw[i] = a;
 }
 
 }  // namespace
 
 cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, cudaStream_t stream) {
     const int64_t n4 = n / 4;
+    // discard needs 128-byte-aligned lines: every s-slice starts at a multiple
+    // of 96 K bytes (K % 8 == 0, so a multiple of 768) from the base
+    const int discard = (reinterpret_cast<uintptr_t>(partial) & 127u) == 0 ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((n4 + kReduceThreads - 1) / kReduceThreads));
     cfg.blockDim = dim3(kReduceThreads);
@@ -60,7 +72,7 @@ cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, cud
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, reduce_dw_kernel, reinterpret_cast<const float4*>(partial),
-                              reinterpret_cast<float4*>(dw), S, n4);
+                              reinterpret_cast<float4*>(dw), S, n4, discard);
 }
 
 }  // namespace mhcpb

@@ -453,18 +453,23 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         uint32_t xph = 0, pph = 0;
         int n_w = 0, prev_strip = -1;
         bool ok = true;
+        // W columns of this lane for the next strip to stage.  They are fetched
+        // a whole strip ahead (right after the current strip is staged), so a
+        // strip change costs no global-memory round trip.
+        float wv[2][kNProj];
+        auto fetch_w = [&](int col0) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int col = col0 + pw * 64 + lane + 32 * q;
+#pragma unroll
+                for (int j = 0; j < kNProj; ++j)
+                    wv[q][j] = col < p.K ? __ldg(p.w + (size_t)j * p.K + col) : 0.f;
+            }
+        };
+        fetch_w(item_at(p, it_begin, u_begin, u_end).col0);
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item I = item_at(p, it, u_begin, u_end);
             if (I.strip != prev_strip) {
-                // W columns of this lane, fetched before waiting for the buffer
-                float wv[2][kNProj];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int col = I.col0 + pw * 64 + lane + 32 * q;
-#pragma unroll
-                    for (int j = 0; j < kNProj; ++j)
-                        wv[q][j] = col < p.K ? __ldg(p.w + (size_t)j * p.K + col) : 0.f;
-                }
                 if (n_w > 0 && !wait_bar(bar(C::B_WE), (uint32_t)(n_w - 1) & 1u, abort_flag,
                                          p.status, tmo, true)) {
                     ok = false;
@@ -487,6 +492,9 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 if (lane == 0) ptx::mbar_arrive(bar(C::B_WF));
                 ++n_w;
                 prev_strip = I.strip;
+                // items are strip-major: the next strip of this CTA, if any, starts
+                // at item (strip + 1) * S
+                if ((I.strip + 1) * p.S < it_end) fetch_w((I.strip + 1) * kStrip);
             }
             for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
                 if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
@@ -536,6 +544,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         const int rr = q * 32 + lane;            // row within the token tile
         const float Kf = static_cast<float>(p.K);
         const uint64_t pol = ptx::policy_evict_first();
+        const uint64_t pol_keep = ptx::policy_evict_last();   // partials: read back by the reduction
         int xs = 0, ab = 0, local = 0;
         uint32_t xph = 0, aph = 0;
         int pend = -1, n = 0;                    // stage whose dX stores may still read smem; tile counter
@@ -664,12 +673,12 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 if (lo_part) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        dst[(size_t)j * p.K] = __uint_as_float(d0[j]) + __uint_as_float(d1[j]);
+                        ptx::st_global_hint(dst + (size_t)j * p.K, __uint_as_float(d0[j]) + __uint_as_float(d1[j]), pol_keep);
                 }
                 if (hi_part) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        dst[(size_t)(16 + i) * p.K] = __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]);
+                        ptx::st_global_hint(dst + (size_t)(16 + i) * p.K, __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]), pol_keep);
                 }
             }
         }

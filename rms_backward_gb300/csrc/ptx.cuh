@@ -77,6 +77,15 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+__device__ __forceinline__ void st_global_hint(float* ptr, float v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(policy)
+                 : "memory");
+}
+// Drops a 128-byte L2 line without writing it back (its contents become undefined).
+__device__ __forceinline__ void discard_l2_line(const void* ptr) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(ptr) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 // 2-D tiled load global -> shared, completion counted on an mbarrier (bytes).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
