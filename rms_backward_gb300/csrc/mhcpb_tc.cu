@@ -73,11 +73,15 @@ struct Cfg {
     static constexpr uint32_t off_w = off_p + NP * kPStage;
     static constexpr uint32_t off_bar = off_w + kWBytes;
     // barriers: x_full[NS] x_empty[NS] p_full[NP] p_empty[NP] acc_full[2]
-    //           acc_empty[2] dw_full[2] dw_empty[2] w_full w_empty fin
+    //           acc_empty[2] dw_full[2] dw_empty[2] w_full w_empty fin side_full[NS]
+    // (side_full: the stage's grad_proj rows, grad_r and r, which come from L2
+    // and land well before the X tile, so P is converted while X is in flight)
     static constexpr int B_XF = 0, B_XE = NS, B_PF = 2 * NS, B_PE = 2 * NS + NP;
     static constexpr int B_AF = 2 * NS + 2 * NP, B_AE = B_AF + 2, B_DF = B_AF + 4,
                          B_DE = B_AF + 6, B_WF = B_AF + 8, B_WE = B_AF + 9, B_FIN = B_AF + 10;
-    static constexpr int n_bars = B_FIN + 1;
+    static constexpr int B_SF = B_FIN + 1;
+    static constexpr uint32_t side_bytes = kPRaw + 2 * kTokenTile * 4;
+    static constexpr int n_bars = B_SF + NS;
     static constexpr uint32_t off_misc = off_bar + n_bars * 8;
     static constexpr uint32_t bytes = off_misc + 16;
     static constexpr uint32_t alloc = bytes + 1024;        // room to align the base to 1 KiB
@@ -132,28 +136,25 @@ __device__ __forceinline__ float tf32_rna(float v) {
     return __uint_as_float(u & 0xFFFFE000u);
 }
 
-// TF32 value -> (hi, lo) BF16 with hi + lo == v exactly (v finite).  A
-// non-finite v keeps lo = 0 so that Inf stays Inf instead of Inf - Inf.
-__device__ __forceinline__ void split_tf32(float v, uint16_t& hi, uint16_t& lo) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    const float rem = isfinite(v) ? v - __bfloat162float(h) : 0.f;
-    const __nv_bfloat16 l = __float2bfloat16_rn(rem);
-    hi = *reinterpret_cast<const uint16_t*>(&h);
-    lo = *reinterpret_cast<const uint16_t*>(&l);
+// TF32 value v -> (hi, lo) BF16 with hi + lo == v exactly (v finite), for two
+// values at once, packed as BF16 pairs (first value in the low half):
+// hi2 = {bf16(a), bf16(b)}, lo2 = {bf16(a - hi_a), bf16(b - hi_b)}; the
+// remainders have at most 4 significant bits, so their rounding is exact.  A
+// non-finite value keeps lo = 0 so that Inf stays Inf instead of Inf - Inf.
+__device__ __forceinline__ void split_tf32x2(float a, float b, uint32_t& hi2, uint32_t& lo2) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    hi2 = *reinterpret_cast<uint32_t*>(&h);
+    float ra = a - __uint_as_float(hi2 << 16);
+    float rb = b - __uint_as_float(hi2 & 0xFFFF0000u);
+    ra = isfinite(a) ? ra : 0.f;
+    rb = isfinite(b) ? rb : 0.f;
+    __nv_bfloat162 l = __floats2bfloat162_rn(ra, rb);
+    lo2 = *reinterpret_cast<uint32_t*>(&l);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint4 pack8(const uint16_t* s) {
-    uint4 v;
-    v.x = s[0] | ((uint32_t)s[1] << 16);
-    v.y = s[2] | ((uint32_t)s[3] << 16);
-    v.z = s[4] | ((uint32_t)s[5] << 16);
-    v.w = s[6] | ((uint32_t)s[7] << 16);
-    return v;
 }
 
 // Work-item geometry shared by all roles.  The schedule unit is half an item
@@ -260,6 +261,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(bar(C::B_XF + s), 1);
             ptx::mbar_init(bar(C::B_XE + s), NEPI);
+            ptx::mbar_init(bar(C::B_SF + s), 1);
         }
         for (int s = 0; s < NP; ++s) {
             ptx::mbar_init(bar(C::B_PF + s), 2);
@@ -318,20 +320,22 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     const int tok0 = I.t_begin + tt * kTokenTile;
                     const uint32_t dst = sbase + (uint32_t)st * C::stage_bytes;
                     const uint32_t fb = bar(C::B_XF + st);
+                    const uint32_t sb = bar(C::B_SF + st);
+                    // side data first (L2-resident, lands early)
+                    ptx::mbar_arrive_expect_tx(sb, C::side_bytes);
+                    ptx::tma_load_2d(dst + C::st_p, &maps.gp, 0, tok0, sb, pol_keep);
+                    ptx::tma_load_2d(dst + C::st_gr, &maps.gr, tok0, 0, sb, pol_keep);
+                    ptx::tma_load_2d(dst + C::st_r, &maps.r, tok0, 0, sb, pol_keep);
                     // only this CTA's 64-column halves of X (and of the addend) are
                     // fetched; the tensor cores still read the whole stage, and the
                     // accumulator rows/columns of a missing half are never used
                     const uint32_t nbox = (I.hmask & 1u) + (I.hmask >> 1);
-                    ptx::mbar_arrive_expect_tx(
-                        fb, C::stage_bytes - (2u - nbox) * kBoxBytes * (ADD ? 2u : 1u));
+                    ptx::mbar_arrive_expect_tx(fb, nbox * kBoxBytes * (ADD ? 2u : 1u));
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
                         if (I.hmask & (1u << h))
                             ptx::tma_load_2d(dst + h * kBoxBytes, &maps.x, I.col0 + h * kBoxCols,
                                              tok0, fb, pol_stream);
-                    ptx::tma_load_2d(dst + C::st_p, &maps.gp, 0, tok0, fb, pol_keep);
-                    ptx::tma_load_2d(dst + C::st_gr, &maps.gr, tok0, 0, fb, pol_keep);
-                    ptx::tma_load_2d(dst + C::st_r, &maps.r, tok0, 0, fb, pol_keep);
                     if (ADD) {
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
@@ -350,9 +354,12 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             }
             // drain: every load this thread issued has landed before the CTA exits
             for (int s = 0; s < NS; ++s)
-                if (issued & (1u << s))
+                if (issued & (1u << s)) {
+                    wait_bar(bar(C::B_SF + s), (last_par >> s) & 1u, abort_flag, p.status, tmo,
+                             false);
                     wait_bar(bar(C::B_XF + s), (last_par >> s) & 1u, abort_flag, p.status, tmo,
                              false);
+                }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -479,13 +486,16 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int cc = pw * 64 + lane + 32 * q;
-                    uint16_t hi[kNProj], lo[kNProj];
+                    uint32_t hw[kNProj / 2], lw[kNProj / 2];   // BF16 pairs (j, j+1)
 #pragma unroll
-                    for (int j = 0; j < kNProj; ++j) split_tf32(tf32_rna(wv[q][j]), hi[j], lo[j]);
-                    const uint16_t* src[8] = {hi, hi + 8, hi + 16, hi + 16, lo, lo + 8, lo + 16, lo + 16};
+                    for (int k = 0; k < kNProj / 2; ++k)
+                        split_tf32x2(tf32_rna(wv[q][2 * k]), tf32_rna(wv[q][2 * k + 1]), hw[k], lw[k]);
+                    // blocks: Wh 0-7, Wh 8-15, Wh 16-23 (twice), Wl 0-7, Wl 8-15, Wl 16-23 (twice)
+                    const uint32_t* src[8] = {hw, hw + 4, hw + 8, hw + 8, lw, lw + 4, lw + 8, lw + 8};
 #pragma unroll
                     for (int wb = 0; wb < 8; ++wb)
-                        *reinterpret_cast<uint4*>(wsm + w_off(cc, wb)) = pack8(src[wb]);
+                        *reinterpret_cast<uint4*>(wsm + w_off(cc, wb)) =
+                            make_uint4(src[wb][0], src[wb][1], src[wb][2], src[wb][3]);
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -497,7 +507,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 if ((I.strip + 1) * p.S < it_end) fetch_w((I.strip + 1) * kStrip);
             }
             for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
-                if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
+                if (!wait_bar(bar(C::B_SF + xs), xph, abort_flag, p.status, tmo, true)) {
                     ok = false;
                     break;
                 }
@@ -518,13 +528,16 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                         const float4 v4 = *reinterpret_cast<const float4*>(praw + tok * kNProj + 4 * q);
                         f[4 * q] = v4.x; f[4 * q + 1] = v4.y; f[4 * q + 2] = v4.z; f[4 * q + 3] = v4.w;
                     }
-                    uint16_t hi[kNProj], lo[kNProj];
+                    uint32_t hw[kNProj / 2], lw[kNProj / 2];   // BF16 pairs (j, j+1)
 #pragma unroll
-                    for (int j = 0; j < kNProj; ++j) split_tf32(tf32_rna(f[j]), hi[j], lo[j]);
-                    const uint16_t* src[6] = {hi, hi + 8, lo, lo + 8, hi + 16, lo + 16};
+                    for (int k = 0; k < kNProj / 2; ++k)
+                        split_tf32x2(tf32_rna(f[2 * k]), tf32_rna(f[2 * k + 1]), hw[k], lw[k]);
+                    // blocks: Ph 0-7, Ph 8-15, Pl 0-7, Pl 8-15, Ph 16-23, Pl 16-23
+                    const uint32_t* src[6] = {hw, hw + 4, lw, lw + 4, hw + 8, lw + 8};
 #pragma unroll
                     for (int jb = 0; jb < 6; ++jb)
-                        *reinterpret_cast<uint4*>(psm + p_off(tok, jb)) = pack8(src[jb]);
+                        *reinterpret_cast<uint4*>(psm + p_off(tok, jb)) =
+                            make_uint4(src[jb][0], src[jb][1], src[jb][2], src[jb][3]);
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
@@ -555,7 +568,8 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             const uint32_t dph = (uint32_t)(local >> 1) & 1u;
             for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
                 const int tok0 = I.t_begin + tt * kTokenTile;
-                if (!wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
+                if (!wait_bar(bar(C::B_SF + xs), xph, abort_flag, p.status, tmo, true) ||
+                    !wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
                     ok = false;
                     break;
                 }
