@@ -22,6 +22,8 @@ struct mhcpb_plan_s {
     int device = 0;
     uint32_t flags = 0;
     int S = 0;            // dW partials
+    int chunk = 0;        // tokens per dW partial
+    int half_units = 0;   // tensor-core kernel schedules half items
     int n_strips = 0;     // strips of the streaming kernel in use
     int grid = 0;         // CTAs of the streaming kernel
     size_t ws_bytes = 0;
@@ -173,7 +175,7 @@ const char* mhcpb_status_string(mhcpb_status_t s) {
         case MHCPB_ERR_DEVICE_TIMEOUT: return "a wait inside the kernel timed out";
         case MHCPB_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3";
         case MHCPB_ERR_SCRATCH_TOO_SMALL:
-            return "shape needs more dW-partial scratch than the built-in 16 MiB buffer";
+            return "shape needs more dW-partial scratch than the built-in 32 MiB buffer";
     }
     return "unknown status";
 }
@@ -218,7 +220,8 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
     p->K = K;
     p->device = device;
     p->flags = flags;
-    p->S = (int)((T + kTokensPerPartial - 1) / kTokensPerPartial);
+    p->chunk = partial_tokens(T);
+    p->S = (int)((T + p->chunk - 1) / p->chunk);
     p->ws_bytes = (size_t)p->S * kNProj * (size_t)K * sizeof(float);
     if (fma_kernel) {
         p->n_strips = (int)((K + fma::kStrip - 1) / fma::kStrip);
@@ -227,6 +230,7 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
     } else {
         p->n_strips = (int)((K + tc::kStrip - 1) / tc::kStrip);
         const int64_t items = (int64_t)p->n_strips * p->S;
+        p->half_units = tc::use_half_units(items, sms) ? 1 : 0;
         p->grid = tc::grid_size(items, sms);
         p->max_grid = p->grid;
         if (const char* ev = std::getenv("MHCPB_EPI_WARPS")) p->epi_warps = std::atoi(ev) == 4 ? 4 : 8;
@@ -284,8 +288,9 @@ mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value) {
         case 3: *value = plan->grid; break;
         case 4: *value = plan->flags; break;
         case 5: *value = (int64_t)plan->smem; break;
-        case 6: *value = (plan->flags & MHCPB_FMA_KERNEL) ? kTokensPerPartial : tc::kTokenTile; break;
+        case 6: *value = (plan->flags & MHCPB_FMA_KERNEL) ? plan->chunk : tc::kTokenTile; break;
         case 7: *value = (plan->flags & MHCPB_FMA_KERNEL) ? fma::kStrip : tc::kStrip; break;
+        case 8: *value = plan->chunk; break;
         default: return MHCPB_ERR_INVALID_ARG;
     }
     return MHCPB_OK;
@@ -332,7 +337,9 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float
     p.T = (int32_t)T;
     p.K = (int32_t)K;
     p.S = plan->S;
+    p.chunk = plan->chunk;
     p.n_strips = plan->n_strips;
+    p.half_units = plan->half_units;
     p.x = static_cast<const uint16_t*>(x);
     p.w = w;
     p.grad_proj = grad_proj;

@@ -1,6 +1,6 @@
 // FP32-FMA (CUDA-core) streaming kernel for the mHC projection/RMS backward.
 //
-// Computes, per (64-column strip, 512-token chunk) block (cuDNN frontend page
+// Computes, per (64-column strip, token chunk) block (cuDNN frontend page
 // "DSv4.1 mHC projection/RMS backward", intro):
 //   dX[t,k]            = sum_j P[t,j] W[j,k] + c[t] X[t,k],  c = grad_r / (r K)
 //   partial[s][j][k]   = sum_{t in chunk s} P[t,j] X[t,k]
@@ -20,7 +20,7 @@ namespace fma {
 
 namespace {
 
-constexpr int kChunk = kTokensPerPartial;
+constexpr int kChunk = kMaxTokensPerPartial;   // shared memory is sized for the largest chunk
 constexpr int kGroups = kThreads / 32;   // row groups; a warp spans 64 columns
 
 __device__ __forceinline__ float tf32_rna(float v) {
@@ -43,8 +43,8 @@ __global__ void __launch_bounds__(kThreads) main_fma_kernel(const MainParams p) 
 
     const int strip = blockIdx.x;
     const int chunk = blockIdx.y;
-    const int t0 = chunk * kChunk;
-    const int nt = min(p.T - t0, kChunk);
+    const int t0 = chunk * p.chunk;
+    const int nt = min(p.T - t0, p.chunk);
     const int K = p.K;
 
     for (int i = threadIdx.x; i < nt * kNProj; i += kThreads) {

@@ -8,7 +8,12 @@ namespace mhcpb {
 
 constexpr int kNProj = 24;          // projection columns used (P = grad_proj[:, :24])
 constexpr int kGradProjCols = 32;   // stored width of grad_proj
-constexpr int kTokensPerPartial = 512;  // tokens per dW partial (fixed chunk)
+// Tokens per dW partial: a function of T alone (never of the GPU), so dW bits
+// depend only on (T, K) and the inputs.  256 keeps items small enough to
+// balance the persistent grid; past 8192 tokens 512 keeps the partials (and
+// the reduction's reads) at most 1/128 of the streamed bytes.
+constexpr int kMaxTokensPerPartial = 512;
+inline int partial_tokens(int64_t T) { return T <= 8192 ? 256 : 512; }
 
 // Device status word values (match mhcpb_status_t).
 constexpr uint32_t kDevOk = 0;
@@ -18,8 +23,10 @@ constexpr uint32_t kDevTimeout = 9;
 struct MainParams {
     int32_t T;
     int32_t K;
-    int32_t S;            // number of dW partials = ceil(T / kTokensPerPartial)
+    int32_t S;            // number of dW partials = ceil(T / chunk)
+    int32_t chunk;        // tokens per dW partial (partial_tokens(T))
     int32_t n_strips;     // ceil(K / strip width) of the kernel in use
+    int32_t half_units;   // tensor-core kernel: schedule in half items (64 columns)
     const uint16_t* x;    // BF16 [T, K] (FMA kernel reads it directly)
     const float* w;       // [24, K]
     const float* grad_proj;  // [T, 32]
@@ -35,7 +42,7 @@ struct MainParams {
 };
 
 // Timeline stamps of a traced build: [grid][kTraceEvents][kTraceTiles] u64.
-constexpr int kTraceEvents = 12;
+constexpr int kTraceEvents = 14;
 constexpr int kTraceTiles = 48;
 
 constexpr uint32_t kTestInjectStall = 1u;
@@ -45,10 +52,16 @@ namespace tc {
 constexpr int kTokenTile = 128;    // MMA M for dX; K-extent of one dW MMA group
 constexpr int kStrip = 128;        // columns per strip: MMA N for dX, M for dW
 constexpr int kBoxCols = 64;       // TMA box width (128 bytes of BF16)
-// Persistent grid: one CTA per SM, at most one per schedule unit (half of a
-// (strip, chunk) item), so every CTA has work.
+// Schedule unit: a whole (strip, chunk) item, or half of one (64 columns) when
+// there are fewer than two items per SM.  Under a saturated HBM every CTA
+// advances at about the same number of tiles per microsecond whatever their
+// width, so balance comes from equal tile counts, i.e. whole items; halves
+// only help to spread small problems over more SMs.
+inline bool use_half_units(int64_t items, int sms) { return items < 2 * (int64_t)sms; }
+// Persistent grid: one CTA per SM, at most one per schedule unit, so every
+// CTA has work.
 inline int grid_size(int64_t items, int sms) {
-    const int64_t units = 2 * items;
+    const int64_t units = use_half_units(items, sms) ? 2 * items : items;
     return (int)(units < sms ? units : sms);
 }
 size_t smem_bytes(bool has_addend, int epi_warps);

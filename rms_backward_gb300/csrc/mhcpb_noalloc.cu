@@ -18,7 +18,7 @@ using namespace mhcpb;
 
 namespace {
 
-// The scratch: dW partials [S][24][K] FP32 for S * K <= 16 MiB / 96 bytes.
+// The scratch: dW partials [S][24][K] FP32 for S * K <= 32 MiB / 96 bytes.
 // Part of the module image, so every device that loads it holds it until exit.
 constexpr size_t kScratchBytes = MHCPB_STATIC_SCRATCH_BYTES;
 __device__ __align__(256) float g_static_scratch[kScratchBytes / sizeof(float)];
@@ -90,7 +90,8 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
     if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND)) != 0) return MHCPB_ERR_INVALID_ARG;
     if (T < 1 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
         return MHCPB_ERR_UNSUPPORTED_SHAPE;
-    const int64_t S = (T + kTokensPerPartial - 1) / kTokensPerPartial;
+    const int chunk = partial_tokens(T);
+    const int64_t S = (T + chunk - 1) / chunk;
     const size_t need = (size_t)S * kNProj * (size_t)K * sizeof(float);
     if (need > kScratchBytes) return MHCPB_ERR_SCRATCH_TOO_SMALL;
     const bool add = (flags & MHCPB_HAS_ADDEND) != 0;
@@ -125,6 +126,7 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
     p.T = (int32_t)T;
     p.K = (int32_t)K;
     p.S = (int32_t)S;
+    p.chunk = chunk;
     p.n_strips = (int32_t)((K + tc::kStrip - 1) / tc::kStrip);
     p.x = static_cast<const uint16_t*>(x);
     p.w = w;
@@ -142,6 +144,7 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
     if (const char* bad = encode_tc_maps(m, T, K, x, dx, add ? grad_x_addend : x, grad_proj, grad_r, r))
         return (mhcpb_status_t)record_cuda_error(cudaErrorInvalidValue, bad);
     const int64_t items = (int64_t)p.n_strips * p.S;
+    p.half_units = tc::use_half_units(items, s.sms) ? 1 : 0;
     const int grid = tc::grid_size(items, s.sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], grid, kEpiWarps, st)) != cudaSuccess)

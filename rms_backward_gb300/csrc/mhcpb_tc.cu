@@ -3,15 +3,15 @@
 // What it computes (cuDNN frontend page "DSv4.1 mHC projection/RMS backward",
 // intro): for every token t and column k,
 //   dX[t,k]          = sum_j P[t,j] W[j,k] + c[t] X[t,k],   c = grad_r / (r K)
-//   partial[s][j][k] = sum_{t in chunk s} P[t,j] X[t,k]      (chunk = 512 tokens)
+//   partial[s][j][k] = sum_{t in chunk s} P[t,j] X[t,k]      (chunk: 256 or 512 tokens)
 // with P = grad_proj[:, :24] and W rounded to TF32 (nearest, ties away) and
 // FP32 accumulation.  The second kernel sums the partials in a fixed order.
 //
 // How, on GB300:
 //  * The grid is persistent (one CTA per SM).  Work items are (128-column
-//    strip, 512-token chunk) pairs in strip-major order; a CTA takes a
-//    contiguous range of them, so W for a strip is staged once per strip.
-//    The chunking depends only on T, so dW bits do not depend on the SM count.
+//    strip, token chunk) pairs in strip-major order; a CTA takes a contiguous
+//    range of them, so W for a strip is staged once per strip.  The chunking
+//    depends only on T, so dW bits do not depend on the SM count.
 //  * One pipeline stage per 128-token tile, filled by TMA: the X tile
 //    (128 x 128 BF16 as two 64-column boxes, 128-byte swizzle, read from HBM
 //    exactly once, L2 evict-first), the tile's 24 used grad_proj columns and
@@ -46,7 +46,6 @@ namespace tc {
 
 namespace {
 
-constexpr int kChunk = kTokensPerPartial;
 constexpr int kNJS = 2 * kNProj;                           // 48 split P columns
 constexpr uint32_t kXTile = kTokenTile * kStrip * 2;       // 32 KiB of BF16
 constexpr uint32_t kBoxBytes = kTokenTile * kBoxCols * 2;  // 16 KiB (one 64-column box)
@@ -127,7 +126,8 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile ui
 #endif
 enum TraceEvent {
     EV_PROD_ISSUE = 0, EV_MMA_XFULL, EV_MMA_PFULL, EV_MMA_ACCEMPTY, EV_MMA_ISSUED, EV_EPI_ACCFULL,
-    EV_EPI_STORED, EV_EPI_RELEASE, EV_PREP_XFULL, EV_PREP_PEMPTY, EV_PREP_DONE, EV_PROD_XEMPTY
+    EV_EPI_STORED, EV_EPI_RELEASE, EV_PREP_XFULL, EV_PREP_PEMPTY, EV_PREP_DONE, EV_PROD_XEMPTY,
+    EV_CTA_START, EV_CTA_END
 };
 
 __device__ __forceinline__ float tf32_rna(float v) {
@@ -157,12 +157,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Work-item geometry shared by all roles.  The schedule unit is half an item
-// (64 of the strip's 128 columns): a CTA owns the contiguous unit range
-// [u_begin, u_end), so its first and last item may be half items (hmask 1 or
-// 2).  Splitting an item by columns leaves every dW partial's bits unchanged:
-// a column's partial depends only on that column's tokens, summed in the same
-// tile order whichever CTA computes it.
+// Work-item geometry shared by all roles.  A CTA owns the contiguous range
+// [u_begin, u_end) of schedule units: whole items, or (p.half_units) halves of
+// items (64 of the strip's 128 columns), in which case its first and last
+// item may be half items (hmask 1 or 2).  Splitting an item by columns leaves
+// every dW partial's bits unchanged: a column's partial depends only on that
+// column's tokens, summed in the same tile order whichever CTA computes it.
 struct Item {
     int strip, chunk, col0, t_begin, ntiles;
     uint32_t hmask;   // bit h set: 64-column half h of the strip belongs to this CTA
@@ -172,10 +172,11 @@ __device__ __forceinline__ Item item_at(const MainParams& p, int it, int u_begin
     r.strip = it / p.S;
     r.chunk = it - r.strip * p.S;
     r.col0 = r.strip * kStrip;
-    r.t_begin = r.chunk * kChunk;
-    const int t_end = min(p.T, r.t_begin + kChunk);
+    r.t_begin = r.chunk * p.chunk;
+    const int t_end = min(p.T, r.t_begin + p.chunk);
     r.ntiles = (t_end - r.t_begin + kTokenTile - 1) / kTokenTile;
-    r.hmask = (2 * it >= u_begin ? 1u : 0u) | (2 * it + 1 < u_end ? 2u : 0u);
+    r.hmask = !p.half_units ? 3u
+                            : (2 * it >= u_begin ? 1u : 0u) | (2 * it + 1 < u_end ? 2u : 0u);
     return r;
 }
 
@@ -251,13 +252,14 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
     auto bar = [&](int i) -> uint32_t { return sbase + C::off_bar + 8u * (uint32_t)i; };
 
     const int n_items = p.n_strips * p.S;
-    const int n_units = 2 * n_items;             // gridDim.x <= n_units (host)
+    const int n_units = p.half_units ? 2 * n_items : n_items;   // gridDim.x <= n_units (host)
     const int u_begin = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
     const int u_end = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
-    const int it_begin = u_begin >> 1;
-    const int it_end = ((u_end - 1) >> 1) + 1;
+    const int it_begin = p.half_units ? u_begin >> 1 : u_begin;
+    const int it_end = p.half_units ? ((u_end - 1) >> 1) + 1 : u_end;
 
     if (threadIdx.x == 0) {
+        TRACE(EV_CTA_START, 0);
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(bar(C::B_XF + s), 1);
             ptx::mbar_init(bar(C::B_XE + s), NEPI);
@@ -705,6 +707,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
+        if (lane == 0) TRACE(EV_CTA_END, 0);
     }
 }
 
