@@ -101,9 +101,9 @@ enum {
 #define MHCPB_NPROJ 24
 #define MHCPB_GRAD_PROJ_COLS 32
 /* Tokens per dW partial: the token reduction is split into
- * S = ceil(T / MHCPB_PARTIAL_TOKENS(T)) fixed chunks.  The chunk size is a
- * function of T alone (never of the GPU): 256 tokens up to T = 8192, else 512. */
-#define MHCPB_PARTIAL_TOKENS(T) ((T) <= 8192 ? 256 : 512)
+ * S = ceil(T / MHCPB_PARTIAL_TOKENS(T)) fixed chunks of 512 tokens, whatever
+ * the GPU, so dW bits depend only on (T, K) and the inputs. */
+#define MHCPB_PARTIAL_TOKENS(T) 512
 
 /* Creates a plan for one shape on one device.  Checks the flags and shape
  * first (no CUDA call is made when they are rejected), then that `device` is
@@ -113,7 +113,7 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
                                  uint32_t flags);
 
 /* Scratch bytes an execute needs: S * 24 * K * 4 with
- * S = ceil(T / MHCPB_PARTIAL_TOKENS(T)) (31,457,280 B at T=4096, K=20480).
+ * S = ceil(T / MHCPB_PARTIAL_TOKENS(T)) (15,728,640 B at T=4096, K=20480).
  * Contents need no initialisation and are dead after the execute (the
  * reduction drops them from L2 without writing them back when the workspace
  * is 128-byte aligned). */
@@ -169,8 +169,8 @@ mhcpb_status_t mhcpb_plan_set_wait_limit(mhcpb_plan_t plan, uint64_t nanoseconds
  * plans.  Applies to executes enqueued after the call. */
 mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas);
 
-/* Size of the library's built-in scratch buffer (see below): 32 MiB. */
-#define MHCPB_STATIC_SCRATCH_BYTES (32u << 20)
+/* Size of the library's built-in scratch buffer (see below): 16 MiB. */
+#define MHCPB_STATIC_SCRATCH_BYTES (16u << 20)
 
 /* The backward for callers that cannot allocate device memory at all: code
  * running inside a host framework that owns every byte of the device heap
@@ -185,10 +185,10 @@ mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas);
  *
  *  - No cudaMalloc, cudaFree or other allocating call is made.  The buffer is
  *    part of the loaded module: every GPU that loads the library holds its
- *    32 MiB until the process exits.
+ *    16 MiB until the process exits.
  *  - Shapes needing more than that are rejected with
  *    MHCPB_ERR_SCRATCH_TOO_SMALL: S * 24 * K * 4 bytes with
- *    S = ceil(T / MHCPB_PARTIAL_TOKENS(T)), i.e. up to T = 4352 at K = 20480.
+ *    S = ceil(T / MHCPB_PARTIAL_TOKENS(T)), i.e. up to T = 4096 at K = 20480.
  *  - Runs on the calling thread's current device; all pointers must be device
  *    memory there, 16-byte aligned and disjoint (same contract and status codes
  *    as mhcpb_execute).  `flags` must contain MHCPB_ALLOW_TF32 and may contain

@@ -34,10 +34,10 @@ MHCPB_TEST_INJECT_STALL = 1 << 30
 MHCPB_NPROJ = 24
 MHCPB_GRAD_PROJ_COLS = 32
 def MHCPB_PARTIAL_TOKENS(T: int) -> int:
-    """Tokens per dW partial (a function of T alone)."""
-    return 256 if T <= 8192 else 512
+    """Tokens per dW partial (fixed: never a function of the GPU)."""
+    return 512
 
-MHCPB_STATIC_SCRATCH_BYTES = 32 << 20
+MHCPB_STATIC_SCRATCH_BYTES = 16 << 20
 
 QUERY = {"T": 0, "K": 1, "S": 2, "grid": 3, "flags": 4, "smem": 5, "token_tile": 6, "strip": 7,
          "partial_tokens": 8}
@@ -163,7 +163,7 @@ def mhcpb_execute_static_scratch(T: int, K: int, flags: int, x: int, w: int, gra
                                  grad_r: int, r: int, dx: int, dw: int,
                                  grad_x_addend: int | None, stream: int | None) -> None:
     """The backward without plan or workspace: dW partials in the library's
-    built-in 32 MiB device buffer (for callers that cannot allocate)."""
+    built-in 16 MiB device buffer (for callers that cannot allocate)."""
     _check(load().mhcpb_execute_static_scratch(int(T), int(K), int(flags), x, w, grad_proj, grad_r,
                                                r, dx, dw, grad_x_addend or None, stream or None),
            "mhcpb_execute_static_scratch")

@@ -175,7 +175,7 @@ const char* mhcpb_status_string(mhcpb_status_t s) {
         case MHCPB_ERR_DEVICE_TIMEOUT: return "a wait inside the kernel timed out";
         case MHCPB_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3";
         case MHCPB_ERR_SCRATCH_TOO_SMALL:
-            return "shape needs more dW-partial scratch than the built-in 32 MiB buffer";
+            return "shape needs more dW-partial scratch than the built-in 16 MiB buffer";
     }
     return "unknown status";
 }

@@ -18,7 +18,7 @@ using namespace mhcpb;
 
 namespace {
 
-// The scratch: dW partials [S][24][K] FP32 for S * K <= 32 MiB / 96 bytes.
+// The scratch: dW partials [S][24][K] FP32 for S * K <= 16 MiB / 96 bytes.
 // Part of the module image, so every device that loads it holds it until exit.
 constexpr size_t kScratchBytes = MHCPB_STATIC_SCRATCH_BYTES;
 __device__ __align__(256) float g_static_scratch[kScratchBytes / sizeof(float)];

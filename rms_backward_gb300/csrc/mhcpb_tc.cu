@@ -258,6 +258,36 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
     const int it_begin = p.half_units ? u_begin >> 1 : u_begin;
     const int it_end = p.half_units ? ((u_end - 1) >> 1) + 1 : u_end;
 
+    // Loads of one tile into stage st: side data first (L2-resident, lands
+    // early) on its own barrier, then this CTA's 64-column halves of X (and of
+    // the addend).  The tensor cores read the whole stage; the accumulator
+    // rows/columns of a missing half are never used.
+    auto issue_tile = [&](const Item& I, int tt, int st, uint64_t pol_stream, uint64_t pol_keep) {
+        const int tok0 = I.t_begin + tt * kTokenTile;
+        const uint32_t dst = sbase + (uint32_t)st * C::stage_bytes;
+        const uint32_t fb = bar(C::B_XF + st);
+        const uint32_t sb = bar(C::B_SF + st);
+        ptx::mbar_arrive_expect_tx(sb, C::side_bytes);
+        ptx::tma_load_2d(dst + C::st_p, &maps.gp, 0, tok0, sb, pol_keep);
+        ptx::tma_load_2d(dst + C::st_gr, &maps.gr, tok0, 0, sb, pol_keep);
+        ptx::tma_load_2d(dst + C::st_r, &maps.r, tok0, 0, sb, pol_keep);
+        const uint32_t nbox = (I.hmask & 1u) + (I.hmask >> 1);
+        ptx::mbar_arrive_expect_tx(fb, nbox * kBoxBytes * (ADD ? 2u : 1u));
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            if (I.hmask & (1u << h))
+                ptx::tma_load_2d(dst + h * kBoxBytes, &maps.x, I.col0 + h * kBoxCols, tok0, fb,
+                                 pol_stream);
+        if (ADD) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (I.hmask & (1u << h))
+                    ptx::tma_load_2d(dst + C::st_add + h * kBoxBytes, &maps.add,
+                                     I.col0 + h * kBoxCols, tok0, fb, pol_stream);
+        }
+    };
+
+    int npre = 0;   // tiles thread 0 (the producer lane) issued before the block-wide sync
     if (threadIdx.x == 0) {
         TRACE(EV_CTA_START, 0);
         for (int s = 0; s < NS; ++s) {
@@ -280,14 +310,21 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         ptx::mbar_init(bar(C::B_FIN), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&maps.x);
         ptx::prefetch_tensormap(&maps.dx);
         ptx::prefetch_tensormap(&maps.gp);
         ptx::prefetch_tensormap(&maps.gr);
         ptx::prefetch_tensormap(&maps.r);
         if (ADD) ptx::prefetch_tensormap(&maps.add);
+        // Fill every stage now (all start empty), so the first loads overlap
+        // the TMEM allocation and the block-wide sync below.
+        const uint64_t pol_stream = ptx::policy_evict_first();
+        const uint64_t pol_keep = ptx::policy_evict_last();
+        for (int it = it_begin; it < it_end && npre < NS; ++it) {
+            const Item I = item_at(p, it, u_begin, u_end);
+            for (int tt = 0; tt < I.ntiles && npre < NS; ++tt, ++npre)
+                issue_tile(I, tt, npre, pol_stream, pol_keep);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
@@ -314,36 +351,14 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             for (int it = it_begin; it < it_end && ok; ++it) {
                 const Item I = item_at(p, it, u_begin, u_end);
                 for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
-                    if (!wait_bar(bar(C::B_XE + st), ph ^ 1u, abort_flag, p.status, tmo, true)) {
-                        ok = false;
-                        break;
-                    }
-                    TRACE(EV_PROD_XEMPTY, n);
-                    const int tok0 = I.t_begin + tt * kTokenTile;
-                    const uint32_t dst = sbase + (uint32_t)st * C::stage_bytes;
-                    const uint32_t fb = bar(C::B_XF + st);
-                    const uint32_t sb = bar(C::B_SF + st);
-                    // side data first (L2-resident, lands early)
-                    ptx::mbar_arrive_expect_tx(sb, C::side_bytes);
-                    ptx::tma_load_2d(dst + C::st_p, &maps.gp, 0, tok0, sb, pol_keep);
-                    ptx::tma_load_2d(dst + C::st_gr, &maps.gr, tok0, 0, sb, pol_keep);
-                    ptx::tma_load_2d(dst + C::st_r, &maps.r, tok0, 0, sb, pol_keep);
-                    // only this CTA's 64-column halves of X (and of the addend) are
-                    // fetched; the tensor cores still read the whole stage, and the
-                    // accumulator rows/columns of a missing half are never used
-                    const uint32_t nbox = (I.hmask & 1u) + (I.hmask >> 1);
-                    ptx::mbar_arrive_expect_tx(fb, nbox * kBoxBytes * (ADD ? 2u : 1u));
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        if (I.hmask & (1u << h))
-                            ptx::tma_load_2d(dst + h * kBoxBytes, &maps.x, I.col0 + h * kBoxCols,
-                                             tok0, fb, pol_stream);
-                    if (ADD) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            if (I.hmask & (1u << h))
-                                ptx::tma_load_2d(dst + C::st_add + h * kBoxBytes, &maps.add,
-                                                 I.col0 + h * kBoxCols, tok0, fb, pol_stream);
+                    if (n >= npre) {   // the first npre tiles went out before the sync
+                        if (!wait_bar(bar(C::B_XE + st), ph ^ 1u, abort_flag, p.status, tmo,
+                                      true)) {
+                            ok = false;
+                            break;
+                        }
+                        TRACE(EV_PROD_XEMPTY, n);
+                        issue_tile(I, tt, st, pol_stream, pol_keep);
                     }
                     TRACE(EV_PROD_ISSUE, n);
                     issued |= 1u << st;

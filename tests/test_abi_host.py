@@ -80,13 +80,9 @@ def test_null_arguments_rejected(lib):
     assert lib.mhcpb_get_device_status(None, ctypes.byref(v), 0) == abi.MHCPB_ERR_INVALID_ARG
 
 
-def test_partial_chunking_depends_on_T_only():
-    # S * 24 * K * 4 with S = ceil(T / chunk(T)): 256-token chunks up to T = 8192,
-    # 512 beyond.  At the training profile that is 31,457,280 bytes, twice the
-    # page's 15,728,640 (512-token chunks), for a better-balanced grid.
-    assert abi.MHCPB_PARTIAL_TOKENS(4096) == 256
-    assert abi.MHCPB_PARTIAL_TOKENS(8192) == 256
-    assert abi.MHCPB_PARTIAL_TOKENS(8193) == 512
+def test_workspace_formula_matches_page_size():
+    # S * 24 * K * 4 with S = ceil(T / 512): 15,728,640 bytes at T=4096, K=20480,
+    # the workspace size the page states for the training profile.
     T, K = 4096, 20480
     S = -(-T // abi.MHCPB_PARTIAL_TOKENS(T))
-    assert S * 24 * K * 4 == 31_457_280 == 2 * 15_728_640
+    assert S * 24 * K * 4 == 15_728_640

@@ -90,11 +90,11 @@ def test_missing_addend_rejected():
 
 def test_plan_facts():
     plan = Plan(4096, 20480)
-    assert plan.workspace_bytes == 31_457_280
-    assert plan.query("S") == 16
-    assert plan.query("partial_tokens") == 256
+    assert plan.workspace_bytes == 15_728_640
+    assert plan.query("S") == 8
+    assert plan.query("partial_tokens") == 512
     assert plan.query("grid") == min(torch.cuda.get_device_properties(0).multi_processor_count,
-                                     160 * 16)
+                                     160 * 8)
     assert plan.query("smem") <= 232448
     plan.close()
     plan = Plan(16384, 20480)

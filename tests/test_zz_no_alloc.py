@@ -2,7 +2,7 @@
 
 It serves callers that cannot allocate device memory at all (a framework that
 owns the whole device heap, plugin code handed only its buffers): no plan, no
-workspace, the dW partials in the library's own 32 MiB __device__ buffer.  Its
+workspace, the dW partials in the library's own 16 MiB __device__ buffer.  Its
 results must agree with the workspace entry point, mhcpb_execute, within the
 tolerances every parity test uses; two calls in a row (different shapes, the
 second with the fused addend) check that sharing the one buffer is harmless.
@@ -31,13 +31,13 @@ def _lib():
 def test_oversized_shapes_rejected_before_any_cuda_call():
     lib = _lib()
     nul = [None] * 9
-    # S * 24 * K * 4 bytes of partials must fit the 32 MiB buffer
+    # S * 24 * K * 4 bytes of partials must fit the 16 MiB buffer
     assert lib.mhcpb_execute_static_scratch(16384, 20480, abi.MHCPB_ALLOW_TF32, *nul) == \
         abi.MHCPB_ERR_SCRATCH_TOO_SMALL
-    # at K = 20480: 17 partials (T <= 4352) fit, 18 do not
-    assert lib.mhcpb_execute_static_scratch(4353, 20480, abi.MHCPB_ALLOW_TF32, *nul) == \
+    # at K = 20480: 8 partials (T <= 4096) fit, 9 do not
+    assert lib.mhcpb_execute_static_scratch(4097, 20480, abi.MHCPB_ALLOW_TF32, *nul) == \
         abi.MHCPB_ERR_SCRATCH_TOO_SMALL
-    for T in (4096, 4352):   # fit: with null pointers the next check rejects them
+    for T in (4000, 4096):   # fit: with null pointers the next check rejects them
         assert lib.mhcpb_execute_static_scratch(T, 20480, abi.MHCPB_ALLOW_TF32, *nul) == \
             abi.MHCPB_ERR_INVALID_ARG
     assert lib.mhcpb_execute_static_scratch(64, 512, 0, *nul) == abi.MHCPB_ERR_TF32_NOT_ALLOWED
@@ -97,7 +97,7 @@ def _bits(dx, dw):
 
 @pytest.mark.gpu
 def test_static_scratch_matches_workspace_entry_point_twice():
-    # first call: the largest shape the buffer holds (training profile, 30 MiB
+    # first call: the largest shape the buffer holds (training profile, 15 MiB
     # of partials); second call right after: another shape with the addend
     calls = [WL.config("training_profile"),
              WL.make("no_alloc_addend", T=777, K=2056, seed=51, addend=True)]
