@@ -47,6 +47,9 @@ def _args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kernel", choices=["tcgen05", "fma"], default="tcgen05")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["training_profile", "long_sublayer", "edge", "fused_addend"],
+                    help="the headline is the training profile; the others are extra lines")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
@@ -245,16 +248,21 @@ def run_ours(args):
 
     from rms_backward_gb300 import Plan, abi
 
-    cfg = WL.CONFIGS[WORKLOAD]
+    cfg = dict(WL.CONFIGS[args.workload])
     T, K = cfg["T"], cfg["K"]
-    wl = WL.make(WORKLOAD, T=T, K=K, seed=cfg["seed"] + 97 * rank)
-    plan = Plan(T, K, local, fma_kernel=(args.kernel == "fma"))
+    cfg["seed"] += 97 * rank           # every replica draws its own inputs
+    wl = WL.make(args.workload, **cfg)
+    has_add = wl.has_addend
+    plan = Plan(T, K, local, addend=has_add, fma_kernel=(args.kernel == "fma"))
 
     pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
     h_x = pin(wl.x.view(np.int16)).view(torch.bfloat16)
     h_w, h_gp, h_gr, h_r = pin(wl.w), pin(wl.grad_proj), pin(wl.grad_r), pin(wl.r)
     x = h_x.to(dev)
     w, gp, gr, r = h_w.to(dev), h_gp.to(dev), h_gr.to(dev), h_r.to(dev)
+    h_add = pin(wl.addend.view(np.int16)).view(torch.bfloat16) if has_add else None
+    add = h_add.to(dev) if has_add else None
+    add_ptr = add.data_ptr() if has_add else None
     dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
     dw = torch.empty((24, K), dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
@@ -265,7 +273,7 @@ def run_ours(args):
     def step():
         abi.mhcpb_execute(plan.handle, x.data_ptr(), w.data_ptr(), gp.data_ptr(), gr.data_ptr(),
                           r.data_ptr(), dx.data_ptr(), dw.data_ptr(), ws.data_ptr(),
-                          plan.workspace_bytes, None, sh)
+                          plan.workspace_bytes, add_ptr, sh)
 
     for _ in range(max(3, args.warmup)):
         flush.fill_(1.0)
@@ -317,7 +325,7 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         mean_ms = float(t.item())
 
-    alg = WL.algorithmic_bytes(T, K)
+    alg = WL.algorithmic_bytes(T, K, addend=has_add)
     value = world * alg / (mean_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
 
@@ -334,7 +342,7 @@ def run_ours(args):
         e2.record(stream)
         st = lib.mhcpb_execute_profiled(
             plan.handle, x.data_ptr(), w.data_ptr(), gp.data_ptr(), gr.data_ptr(), r.data_ptr(),
-            dx.data_ptr(), dw.data_ptr(), ws.data_ptr(), plan.workspace_bytes, None, sh,
+            dx.data_ptr(), dw.data_ptr(), ws.data_ptr(), plan.workspace_bytes, add_ptr, sh,
             e0.cuda_event, e1.cuda_event, e2.cuda_event)
         if st != 0:
             raise RuntimeError(f"mhcpb_execute_profiled: {abi.status_string(st)}")
@@ -350,6 +358,7 @@ def run_ours(args):
     h_dx = torch.empty((T, K), dtype=torch.bfloat16).pin_memory()
     h_dw = torch.empty((24, K), dtype=torch.float32).pin_memory()
     h2d = x.numel() * 2 + w.numel() * 4 + gp.numel() * 4 + gr.numel() * 4 + r.numel() * 4
+    h2d += add.numel() * 2 if has_add else 0
     d2h = dx.numel() * 2 + dw.numel() * 4
     for _ in range(3):
         x.copy_(h_x, non_blocking=True)
@@ -366,6 +375,8 @@ def run_ours(args):
         gp.copy_(h_gp, non_blocking=True)
         gr.copy_(h_gr, non_blocking=True)
         r.copy_(h_r, non_blocking=True)
+        if has_add:
+            add.copy_(h_add, non_blocking=True)
         step()
         h_dx.copy_(dx, non_blocking=True)
         h_dw.copy_(dw, non_blocking=True)
@@ -379,21 +390,26 @@ def run_ours(args):
     e2e_value = world * alg / (e2e_ms * 1e-3) / 1e9
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
         gbs, toks, secs = _oracle_rate(T, K, seconds=12.0)
         cpu = {"value": gbs, "unit": "GB/s", "cores": _cpu_threads(), "kind": "oracle",
                "sample": f"{toks} of {T} tokens x K={K} of the training profile "
                          f"(512-token slices, {secs:.1f} s)"}
 
+    metric = METRIC if args.workload == WORKLOAD else \
+        f"mHC proj-bwd achieved HBM GB/s at T={T}, K={K} ({args.workload})"
+    desc = {"training_profile": "training profile", "long_sublayer": "long sublayer",
+            "edge": "edge (rows scaled 10^U(-3,3), grad_proj[:, 24:] = +-1e30)",
+            "fused_addend": "training profile with the fused BF16 addend"}[args.workload]
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "metric": metric, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": mean_ms, "us_per_step": mean_ms * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"training profile T={T} K={K} (4 streams x hidden 5120)",
-                       "T": T, "K": K, "kernel": args.kernel,
+            "config": {"workload": f"{desc} T={T} K={K} (4 streams x hidden 5120)",
+                       "T": T, "K": K, "kernel": args.kernel, "addend": has_add,
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "l2": "flushed before every timed step (256 MiB write, outside the events)",
                        "algorithmic_bytes_per_step": alg,
