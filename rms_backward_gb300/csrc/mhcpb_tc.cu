@@ -79,10 +79,8 @@ struct Cfg {
     static constexpr int B_AF = 2 * NS + 2 * NP, B_AE = B_AF + 2, B_DF = B_AF + 4,
                          B_DE = B_AF + 6, B_WF = B_AF + 8, B_WE = B_AF + 9, B_FIN = B_AF + 10;
     static constexpr int B_SF = B_FIN + 1;
-    // x_done[NS]: the tile's dW MMAs (the last readers of X) have completed
-    static constexpr int B_XD = B_SF + NS;
     static constexpr uint32_t side_bytes = kPRaw + 2 * kTokenTile * 4;
-    static constexpr int n_bars = B_XD + NS;
+    static constexpr int n_bars = B_SF + NS;
     static constexpr uint32_t off_misc = off_bar + n_bars * 8;
     static constexpr uint32_t bytes = off_misc + 16;
     static constexpr uint32_t alloc = bytes + 1024;        // room to align the base to 1 KiB
@@ -204,12 +202,10 @@ struct Maps {
 };
 
 // One 32-column chunk of the dX epilogue for this thread's row: acc (from
-// TMEM) + c * x, BF16 rounding, optional BF16 addend, into o[16] (4 x 16
-// bytes, one per 8 columns).
+// TMEM) + c * x, BF16 rounding, optional BF16 addend, written over x in place.
 template <bool ADD>
-__device__ __forceinline__ void epi_compute(const uint32_t (&v)[32], float c, const uint8_t* xrow,
-                                            const uint8_t* arow, int rr, int sub,
-                                            uint32_t (&out)[16]) {
+__device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], float c, uint8_t* xrow,
+                                          const uint8_t* arow, int rr, int sub) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int ch = sub * 4 + i;
@@ -236,19 +232,7 @@ __device__ __forceinline__ void epi_compute(const uint32_t (&v)[32], float c, co
                 o[e] = pack_bf16x2(s0, s1);
             }
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) out[i * 4 + e] = o[e];
-    }
-}
-
-// Writes a chunk computed by epi_compute over the X tile in place (same
-// swizzled positions it was read from).
-__device__ __forceinline__ void epi_store(uint8_t* xrow, int rr, int sub, const uint32_t (&out)[16]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t off = (uint32_t)(((sub * 4 + i) ^ (rr & 7)) << 4);
-        *reinterpret_cast<uint4*>(xrow + off) =
-            make_uint4(out[i * 4], out[i * 4 + 1], out[i * 4 + 2], out[i * 4 + 3]);
+        *reinterpret_cast<uint4*>(xrow + off) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -310,7 +294,6 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             ptx::mbar_init(bar(C::B_XF + s), 1);
             ptx::mbar_init(bar(C::B_XE + s), NEPI);
             ptx::mbar_init(bar(C::B_SF + s), 1);
-            ptx::mbar_init(bar(C::B_XD + s), 1);
         }
         for (int s = 0; s < NP; ++s) {
             ptx::mbar_init(bar(C::B_PF + s), 2);
@@ -458,9 +441,6 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                                                             ptx::kLayoutInterleave);
                         ptx::mma_bf16(d_dx, da, dbd, idesc_dx, k > 0 ? 1u : 0u);
                     }
-                    // the epilogue may start on the dX accumulator now; it waits for
-                    // x_done before it writes dX over the X tile the dW MMAs read
-                    ptx::tc_commit(bar(C::B_AF + ab));
                     // dW^T += X^T [Ph Pl]: M=128 cols, N=48, K=128 tokens in 8 steps
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -471,7 +451,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                         ptx::mma_bf16(d_dw, da, dbd, idesc_dw, (tt > 0 || k > 0) ? 1u : 0u);
                     }
                     ptx::tc_commit(bar(C::B_PE + ps));
-                    ptx::tc_commit(bar(C::B_XD + xs));
+                    ptx::tc_commit(bar(C::B_AF + ab));
                     TRACE(EV_MMA_ISSUED, n);
                     if (++xs == NS) { xs = 0; xph ^= 1u; }
                     if (++ps == NP) { ps = 0; pph ^= 1u; }
@@ -597,7 +577,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         const uint64_t pol_keep = ptx::policy_evict_last();   // partials: read back by the reduction
         int xs = 0, ab = 0, local = 0;
         uint32_t xph = 0, aph = 0;
-        int n = 0;                               // tile counter of this CTA (trace index)
+        int pend = -1, n = 0;                    // stage whose dX stores may still read smem; tile counter
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it, ++local) {
             const Item I = item_at(p, it, u_begin, u_end);
@@ -622,12 +602,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 const bool mine = (C::HPW == 2) ? (I.hmask != 0u) : (((I.hmask >> h0) & 1u) != 0u);
                 if (!mine) {
                     // none of this warp's columns belong to this CTA in this item:
-                    // only hand the accumulator and (once the dW MMAs are done
-                    // reading it) the stage back
-                    if (!wait_bar(bar(C::B_XD + xs), xph, abort_flag, p.status, tmo, true)) {
-                        ok = false;
-                        break;
-                    }
+                    // only hand the accumulator and the stage back
                     __syncwarp();
                     if (lane == 0) {
                         ptx::mbar_arrive(bar(C::B_AE + ab));
@@ -661,16 +636,10 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                         if (lane == 0) ptx::mbar_arrive(bar(C::B_AE + ab));
                     }
                     const bool hv = ((I.hmask >> h) & 1u) != 0u;   // this half is the CTA's
-                    uint32_t out[16];
                     if (hv) {
-                        if (ch & 1) epi_compute<ADD>(vb, c, xrow, arow, rr, sub, out);
-                        else epi_compute<ADD>(va, c, xrow, arow, rr, sub, out);
+                        if (ch & 1) epi_chunk<ADD>(vb, c, xrow, arow, rr, sub);
+                        else epi_chunk<ADD>(va, c, xrow, arow, rr, sub);
                     }
-                    if (ch == 0 &&
-                        !wait_bar(bar(C::B_XD + xs), xph, abort_flag, p.status, tmo, true)) {
-                        ok = false;   // (the X tile is still read by the dW MMAs until x_done)
-                    }
-                    if (hv && ok) epi_store(xrow, rr, sub, out);
                     if (ch + 1 < nch) {
                         if (ch & 1) ptx::tc_wait_ld_regs(va);
                         else ptx::tc_wait_ld_regs(vb);
@@ -678,20 +647,27 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     if (sub == 1) {
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0 && ok && hv && tok0 + q * 32 < p.T && I.col0 + h * kBoxCols < p.K)
+                        if (lane == 0 && hv && tok0 + q * 32 < p.T && I.col0 + h * kBoxCols < p.K)
                             ptx::tma_store_2d(&maps.dx, ptx::smem_u32(xst + h * kBoxBytes + q * 32 * 128),
                                               I.col0 + h * kBoxCols, tok0 + q * 32, pol);
                     }
                 }
-                if (!ok) break;
                 if (lane == 0) {
                     ptx::bulk_commit();
                     if (e == 0) TRACE(EV_EPI_STORED, n);
+#ifdef MHCPB_DEFER_RELEASE
+                    if (pend >= 0) {
+                        ptx::bulk_wait_read<1>();      // the previous tile's stores have read smem
+                        ptx::mbar_arrive(bar(C::B_XE + pend));
+                    }
+#else
                     ptx::bulk_wait_read<0>();          // this tile's stores have read smem
                     ptx::mbar_arrive(bar(C::B_XE + xs));
+#endif
                     if (e == 0) TRACE(EV_EPI_RELEASE, n);
                 }
                 __syncwarp();
+                pend = xs;
                 if (++xs == NS) { xs = 0; xph ^= 1u; }
                 if (++ab == 2) { ab = 0; aph ^= 1u; }
             }
