@@ -42,7 +42,7 @@ struct MainParams {
 };
 
 // Timeline stamps of a traced build: [grid][kTraceEvents][kTraceTiles] u64.
-constexpr int kTraceEvents = 14;
+constexpr int kTraceEvents = 16;
 constexpr int kTraceTiles = 48;
 
 constexpr uint32_t kTestInjectStall = 1u;

@@ -3,7 +3,7 @@
 // What it computes (cuDNN frontend page "DSv4.1 mHC projection/RMS backward",
 // intro): for every token t and column k,
 //   dX[t,k]          = sum_j P[t,j] W[j,k] + c[t] X[t,k],   c = grad_r / (r K)
-//   partial[s][j][k] = sum_{t in chunk s} P[t,j] X[t,k]      (chunk: 256 or 512 tokens)
+//   partial[s][j][k] = sum_{t in chunk s} P[t,j] X[t,k]      (chunk: 512 tokens)
 // with P = grad_proj[:, :24] and W rounded to TF32 (nearest, ties away) and
 // FP32 accumulation.  The second kernel sums the partials in a fixed order.
 //
@@ -72,12 +72,14 @@ struct Cfg {
     static constexpr uint32_t off_w = off_p + NP * kPStage;
     static constexpr uint32_t off_bar = off_w + kWBytes;
     // barriers: x_full[NS] x_empty[NS] p_full[NP] p_empty[NP] acc_full[2]
-    //           acc_empty[2] dw_full[2] dw_empty[2] w_full w_empty fin side_full[NS]
+    //           acc_empty[2] dw_empty[2] w_full w_empty fin side_full[NS]
+    // (no dw_full: an item's dW accumulator is final when its last tile's
+    // acc_full completes, which tracks the same MMAs)
     // (side_full: the stage's grad_proj rows, grad_r and r, which come from L2
     // and land well before the X tile, so P is converted while X is in flight)
     static constexpr int B_XF = 0, B_XE = NS, B_PF = 2 * NS, B_PE = 2 * NS + NP;
-    static constexpr int B_AF = 2 * NS + 2 * NP, B_AE = B_AF + 2, B_DF = B_AF + 4,
-                         B_DE = B_AF + 6, B_WF = B_AF + 8, B_WE = B_AF + 9, B_FIN = B_AF + 10;
+    static constexpr int B_AF = 2 * NS + 2 * NP, B_AE = B_AF + 2, B_DE = B_AF + 4,
+                         B_WF = B_AF + 6, B_WE = B_AF + 7, B_FIN = B_AF + 8;
     static constexpr int B_SF = B_FIN + 1;
     static constexpr uint32_t side_bytes = kPRaw + 2 * kTokenTile * 4;
     static constexpr int n_bars = B_SF + NS;
@@ -127,7 +129,7 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile ui
 enum TraceEvent {
     EV_PROD_ISSUE = 0, EV_MMA_XFULL, EV_MMA_PFULL, EV_MMA_ACCEMPTY, EV_MMA_ISSUED, EV_EPI_ACCFULL,
     EV_EPI_STORED, EV_EPI_RELEASE, EV_PREP_XFULL, EV_PREP_PEMPTY, EV_PREP_DONE, EV_PROD_XEMPTY,
-    EV_CTA_START, EV_CTA_END
+    EV_CTA_START, EV_CTA_END, EV_DRAIN_START, EV_DRAIN_END   // drains indexed by item
 };
 
 __device__ __forceinline__ float tf32_rna(float v) {
@@ -302,7 +304,6 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(C::B_AF + b), 1);
             ptx::mbar_init(bar(C::B_AE + b), NEPI);
-            ptx::mbar_init(bar(C::B_DF + b), 1);
             ptx::mbar_init(bar(C::B_DE + b), NEPI);
         }
         ptx::mbar_init(bar(C::B_WF), 2);
@@ -458,7 +459,6 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     if (++ab == 2) { ab = 0; aph ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::tc_commit(bar(C::B_DF + db));
                 const int next_strip = (it + 1 < it_end) ? (it + 1) / p.S : -1;
                 if (next_strip != I.strip) ptx::tc_commit(bar(C::B_WE));
                 prev_strip = I.strip;
@@ -577,14 +577,43 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         const uint64_t pol_keep = ptx::policy_evict_last();   // partials: read back by the reduction
         int xs = 0, ab = 0, local = 0;
         uint32_t xph = 0, aph = 0;
-        int pend = -1, n = 0;                    // stage whose dX stores may still read smem; tile counter
+        int n = 0;                               // tile counter (trace index)
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it, ++local) {
             const Item I = item_at(p, it, u_begin, u_end);
             const int db = local & 1;
-            const uint32_t dph = (uint32_t)(local >> 1) & 1u;
+            // dW partial of this item: this warp's lanes are strip columns
+            // 32q..32q+31 (TMEM lane quarter q), i.e. half q / 2 of the strip
+            const bool cols_mine = ((I.hmask >> (q >> 1)) & 1u) != 0u;
+            const bool lo_part = cols_mine && ((C::HPW == 2) || h0 == 0);   // j 0..15
+            const bool hi_part = cols_mine && ((C::HPW == 2) || h0 == 1);   // j 16..23
+            const uint32_t dcol = tmem + lane_base + kDwCol + (uint32_t)db * kDwColStride;
+            uint32_t d0[16], d1[16], d2[16];
+            // Stores this thread's columns of the partial (after the last tile's
+            // stage went back to the producer, so they delay no X load).
+            auto store_partial = [&]() {
+                if (e == 0 && lane == 0) TRACE(EV_DRAIN_START, local);
+                const int col = I.col0 + q * 32 + lane;
+                if (col < p.K) {
+                    float* dst = p.partial + (size_t)I.chunk * kNProj * p.K + col;
+                    // accumulator columns: 0-15 X^T Ph[0..15], 16-31 X^T Pl[0..15],
+                    //                      32-39 X^T Ph[16..23], 40-47 X^T Pl[16..23]
+                    if (lo_part) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            ptx::st_global_hint(dst + (size_t)j * p.K, __uint_as_float(d0[j]) + __uint_as_float(d1[j]), pol_keep);
+                    }
+                    if (hi_part) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            ptx::st_global_hint(dst + (size_t)(16 + i) * p.K, __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]), pol_keep);
+                    }
+                }
+                if (e == 0 && lane == 0) TRACE(EV_DRAIN_END, local);
+            };
             for (int tt = 0; tt < I.ntiles; ++tt, ++n) {
                 const int tok0 = I.t_begin + tt * kTokenTile;
+                const bool last = tt == I.ntiles - 1;
                 if (!wait_bar(bar(C::B_SF + xs), xph, abort_flag, p.status, tmo, true) ||
                     !wait_bar(bar(C::B_XF + xs), xph, abort_flag, p.status, tmo, true)) {
                     ok = false;
@@ -599,25 +628,53 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     break;
                 }
                 if (e == 0 && lane == 0) TRACE(EV_EPI_ACCFULL, n);
+                ptx::tc_fence_after();
+                if (last) {
+                    // the MMAs whose completion ACC_FULL signalled include the item's
+                    // last dW MMAs: the dW accumulator is final; read it now, together
+                    // with the first dX columns
+                    if (lo_part) {
+                        ptx::tmem_ld_32x32b_x16(dcol, d0);
+                        ptx::tmem_ld_32x32b_x16(dcol + 16, d1);
+                    }
+                    if (hi_part) ptx::tmem_ld_32x32b_x16(dcol + 32, d2);
+                }
                 const bool mine = (C::HPW == 2) ? (I.hmask != 0u) : (((I.hmask >> h0) & 1u) != 0u);
                 if (!mine) {
-                    // none of this warp's columns belong to this CTA in this item:
-                    // only hand the accumulator and the stage back
+                    // none of this warp's dX columns belong to this CTA in this item:
+                    // only hand the accumulator(s) and the stage back
+                    if (last) {
+                        ptx::tc_wait_ld();
+                        ptx::reg_fence16(d0);
+                        ptx::reg_fence16(d1);
+                        ptx::reg_fence16(d2);
+                        ptx::tc_fence_before();
+                    }
                     __syncwarp();
                     if (lane == 0) {
                         ptx::mbar_arrive(bar(C::B_AE + ab));
                         ptx::mbar_arrive(bar(C::B_XE + xs));
+                        if (last) ptx::mbar_arrive(bar(C::B_DE + db));
                     }
                     __syncwarp();
                     if (++xs == NS) { xs = 0; xph ^= 1u; }
                     if (++ab == 2) { ab = 0; aph ^= 1u; }
+                    if (last) store_partial();
                     continue;
                 }
-                ptx::tc_fence_after();
                 const uint32_t tcol = tmem + lane_base + (uint32_t)ab * kStrip + (uint32_t)(h0 * 64);
                 uint32_t va[32], vb[32];
                 ptx::tmem_ld_32x32b_x32(tcol, va);
-                ptx::tc_wait_ld_regs(va);
+                ptx::tc_wait_ld_regs(va);   // (and the dW columns)
+                if (last) {
+                    ptx::reg_fence16(d0);
+                    ptx::reg_fence16(d1);
+                    ptx::reg_fence16(d2);
+                    // the dW accumulator is in registers: the MMA issuer may reuse it
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(C::B_DE + db));
+                }
                 constexpr int nch = 2 * C::HPW;   // 32-column chunks of this warp
 #pragma unroll
                 for (int ch = 0; ch < nch; ++ch) {
@@ -655,62 +712,14 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 if (lane == 0) {
                     ptx::bulk_commit();
                     if (e == 0) TRACE(EV_EPI_STORED, n);
-#ifdef MHCPB_DEFER_RELEASE
-                    if (pend >= 0) {
-                        ptx::bulk_wait_read<1>();      // the previous tile's stores have read smem
-                        ptx::mbar_arrive(bar(C::B_XE + pend));
-                    }
-#else
                     ptx::bulk_wait_read<0>();          // this tile's stores have read smem
                     ptx::mbar_arrive(bar(C::B_XE + xs));
-#endif
                     if (e == 0) TRACE(EV_EPI_RELEASE, n);
                 }
                 __syncwarp();
-                pend = xs;
                 if (++xs == NS) { xs = 0; xph ^= 1u; }
                 if (++ab == 2) { ab = 0; aph ^= 1u; }
-            }
-            if (!ok) break;
-            // dW partial of this chunk: lane = column of the strip
-            if (!wait_bar(bar(C::B_DF + db), dph, abort_flag, p.status, tmo, true)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            uint32_t d0[16], d1[16], d2[16];
-            const uint32_t dcol = tmem + lane_base + kDwCol + (uint32_t)db * kDwColStride;
-            // this warp's lanes are strip columns 32q..32q+31, i.e. half q / 2
-            const bool cols_mine = ((I.hmask >> (q >> 1)) & 1u) != 0u;
-            const bool lo_part = cols_mine && ((C::HPW == 2) || h0 == 0);   // j 0..15
-            const bool hi_part = cols_mine && ((C::HPW == 2) || h0 == 1);   // j 16..23
-            if (lo_part) {
-                ptx::tmem_ld_32x32b_x16(dcol, d0);
-                ptx::tmem_ld_32x32b_x16(dcol + 16, d1);
-            }
-            if (hi_part) ptx::tmem_ld_32x32b_x16(dcol + 32, d2);
-            ptx::tc_wait_ld();
-            ptx::reg_fence16(d0);
-            ptx::reg_fence16(d1);
-            ptx::reg_fence16(d2);
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(C::B_DE + db));
-            const int col = I.col0 + q * 32 + lane;
-            if (col < p.K) {
-                float* dst = p.partial + (size_t)I.chunk * kNProj * p.K + col;
-                // accumulator columns: 0-15 X^T Ph[0..15], 16-31 X^T Pl[0..15],
-                //                      32-39 X^T Ph[16..23], 40-47 X^T Pl[16..23]
-                if (lo_part) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        ptx::st_global_hint(dst + (size_t)j * p.K, __uint_as_float(d0[j]) + __uint_as_float(d1[j]), pol_keep);
-                }
-                if (hi_part) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        ptx::st_global_hint(dst + (size_t)(16 + i) * p.K, __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]), pol_keep);
-                }
+                if (last) store_partial();
             }
         }
         if (lane == 0) ptx::bulk_wait<0>();   // all dX stores of this warp are complete
