@@ -50,6 +50,8 @@ def _args():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["training_profile", "long_sublayer", "edge", "fused_addend"],
                     help="the headline is the training profile; the others are extra lines")
+    ap.add_argument("--compensated-dw", action="store_true",
+                    help="plan flag MHCPB_COMPENSATED_DW (TwoSum dW reduction, one rounding)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
@@ -253,7 +255,8 @@ def run_ours(args):
     cfg["seed"] += 97 * rank           # every replica draws its own inputs
     wl = WL.make(args.workload, **cfg)
     has_add = wl.has_addend
-    plan = Plan(T, K, local, addend=has_add, fma_kernel=(args.kernel == "fma"))
+    plan = Plan(T, K, local, addend=has_add, fma_kernel=(args.kernel == "fma"),
+                compensated_dw=args.compensated_dw)
 
     pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
     h_x = pin(wl.x.view(np.int16)).view(torch.bfloat16)
@@ -410,6 +413,7 @@ def run_ours(args):
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"{desc} T={T} K={K} (4 streams x hidden 5120)",
                        "T": T, "K": K, "kernel": args.kernel, "addend": has_add,
+                       "dw_reduction": "compensated" if args.compensated_dw else "plain",
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "l2": "flushed before every timed step (256 MiB write, outside the events)",
                        "algorithmic_bytes_per_step": alg,

@@ -86,6 +86,22 @@ enum {
      * one.  Same results within tolerance, same determinism; kept as the
      * measured control for the tensor-core kernel. */
     MHCPB_FMA_KERNEL = 4u,
+    /* Compensated dW reduction: the second kernel sums each element's S chunk
+     * partials in the same fixed order, but with an error-free transformation
+     * at every addition (TwoSum: s + p = s' + e exactly) and the errors e
+     * accumulated beside the sum, then rounds once to FP32: dW = fl(s + E).
+     * This is Ogita, Rump and Oishi's cascaded summation (Sum2): as accurate
+     * as summing the partials in twice the working precision and rounding
+     * once, instead of S - 1 FP32 roundings.  Within a
+     * chunk the products are exact in either mode (TF32 x BF16 split into
+     * BF16 pairs) and are accumulated by the tensor cores in FP32.  Same
+     * determinism: bitwise reproducible and independent of the SM count.
+     * The idea comes from the FlashInfer page on
+     * cake_rmsnorm_det_train_backward (program windows), whose small-T dw
+     * column sums keep exact products, accumulate with TwoSum and round to
+     * FP32 once; here it is applied to the cross-chunk reduction.  Costs a
+     * few FP32 operations per partial in the second kernel only. */
+    MHCPB_COMPENSATED_DW = 8u,
     /* Test hook for failure detection: in the tensor-core kernel the MMA
      * issuer first waits on a barrier that nothing completes, so the execute
      * ends by the in-kernel wait limit, records MHCPB_ERR_DEVICE_TIMEOUT in the
@@ -192,7 +208,8 @@ mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas);
  *  - Runs on the calling thread's current device; all pointers must be device
  *    memory there, 16-byte aligned and disjoint (same contract and status codes
  *    as mhcpb_execute).  `flags` must contain MHCPB_ALLOW_TF32 and may contain
- *    MHCPB_HAS_ADDEND (then `grad_x_addend` is required), nothing else.
+ *    MHCPB_HAS_ADDEND (then `grad_x_addend` is required) and
+ *    MHCPB_COMPENSATED_DW, nothing else.
  *  - The first call on a device does that device's set-up (looks up the
  *    buffer's device address, raises the kernels' shared-memory limit).  Make
  *    that first call before any stream capture.

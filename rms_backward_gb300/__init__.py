@@ -14,7 +14,8 @@ from __future__ import annotations
 
 from . import abi
 from .abi import (  # noqa: F401
-    MHCPB_ALLOW_TF32, MHCPB_FMA_KERNEL, MHCPB_HAS_ADDEND, MhcpbError, mhcpb_destroy,
+    MHCPB_ALLOW_TF32, MHCPB_COMPENSATED_DW, MHCPB_FMA_KERNEL, MHCPB_HAS_ADDEND, MhcpbError,
+    mhcpb_destroy,
     mhcpb_execute, mhcpb_get_device_status, mhcpb_last_cuda_error, mhcpb_plan_create,
     mhcpb_plan_query, mhcpb_plan_set_max_ctas, mhcpb_plan_set_wait_limit, mhcpb_status_string,
     mhcpb_workspace_bytes,
@@ -25,8 +26,11 @@ class Plan:
     """A prepared backward for one (T, K) on one device (owns a C plan handle)."""
 
     def __init__(self, T: int, K: int, device: int = 0, *, addend: bool = False,
-                 fma_kernel: bool = False, test_inject_stall: bool = False):
+                 fma_kernel: bool = False, compensated_dw: bool = False,
+                 test_inject_stall: bool = False):
         flags = abi.MHCPB_ALLOW_TF32
+        if compensated_dw:
+            flags |= abi.MHCPB_COMPENSATED_DW
         if test_inject_stall:
             flags |= abi.MHCPB_TEST_INJECT_STALL
         if addend:
@@ -75,7 +79,7 @@ class Plan:
 
 
 def mhc_projection_backward(x, weight, grad_proj, grad_r, r, addend=None, *, stream=None,
-                            fma_kernel: bool = False):
+                            fma_kernel: bool = False, compensated_dw: bool = False):
     """Allocating convenience call: returns (dx BF16 [T,K], dw FP32 [24,K]).
 
     Outputs and workspace are allocated by torch on the tensors' device.  The
@@ -83,7 +87,8 @@ def mhc_projection_backward(x, weight, grad_proj, grad_r, r, addend=None, *, str
     """
     import torch
     T, K = x.shape
-    plan = Plan(T, K, x.device.index or 0, addend=addend is not None, fma_kernel=fma_kernel)
+    plan = Plan(T, K, x.device.index or 0, addend=addend is not None, fma_kernel=fma_kernel,
+                compensated_dw=compensated_dw)
     dx = torch.empty((T, K), dtype=torch.bfloat16, device=x.device)
     dw = torch.empty((24, K), dtype=torch.float32, device=x.device)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=x.device)

@@ -29,6 +29,7 @@ MHCPB_ERR_SCRATCH_TOO_SMALL = 11
 MHCPB_ALLOW_TF32 = 1
 MHCPB_HAS_ADDEND = 2
 MHCPB_FMA_KERNEL = 4
+MHCPB_COMPENSATED_DW = 8
 MHCPB_TEST_INJECT_STALL = 1 << 30
 
 MHCPB_NPROJ = 24

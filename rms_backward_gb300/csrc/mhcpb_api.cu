@@ -187,7 +187,7 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
     if (out == nullptr) return MHCPB_ERR_INVALID_ARG;
     if ((flags & MHCPB_ALLOW_TF32) == 0) return MHCPB_ERR_TF32_NOT_ALLOWED;
     if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND | MHCPB_FMA_KERNEL |
-                            MHCPB_TEST_INJECT_STALL)) != 0)
+                            MHCPB_COMPENSATED_DW | MHCPB_TEST_INJECT_STALL)) != 0)
         return MHCPB_ERR_INVALID_ARG;
     if (T < 1 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
         return MHCPB_ERR_UNSUPPORTED_SHAPE;
@@ -369,7 +369,8 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float
     }
     if (ev1 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev1), st)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord");
-    e = launch_reduce(p.partial, dw, plan->S, (int64_t)kNProj * K, st);
+    e = launch_reduce(p.partial, dw, plan->S, (int64_t)kNProj * K,
+                      (plan->flags & MHCPB_COMPENSATED_DW) != 0, st);
     if (e != cudaSuccess) return cuda_fail(e, "launch (dW reduction)");
     if (ev2 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev2), st)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord");

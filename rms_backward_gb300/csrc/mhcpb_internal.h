@@ -90,7 +90,9 @@ const char* encode_tc_maps(CUtensorMap (&m)[6], int64_t T, int64_t K, const void
                            const void* r);
 int record_cuda_error(cudaError_t e, const char* what);
 
-// Second kernel: dW[j,k] = sum over s ascending of partial[s][j][k].
-cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, cudaStream_t stream);
+// Second kernel: dW[j,k] = sum over s ascending of partial[s][j][k]; with
+// `compensated`, TwoSum at every addition and one final rounding.
+cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, bool compensated,
+                          cudaStream_t stream);
 
 }  // namespace mhcpb

@@ -7,7 +7,15 @@
 //   dW[j,k] = (((partial[0][j][k] + partial[1][j][k]) + partial[2][j][k]) + ...)
 //
 // One thread owns four consecutive dW elements; the sum runs over s in
-// ascending order, so dW depends only on (T, K) and the inputs.  Launched as a
+// ascending order, so dW depends only on (T, K) and the inputs.
+//
+// Compensated variant (plan flag MHCPB_COMPENSATED_DW): the same order, with
+// Knuth's TwoSum at every addition, s + p = s' + e exactly (six FP32
+// additions, no branch), the errors e summed beside s and added once at the
+// end -- Ogita, Rump and Oishi's Sum2, which is as accurate as the sum in
+// twice the working precision rounded once.  FlashInfer's page on
+// cake_rmsnorm_det_train_backward describes the same idea for its small-T dw
+// column sums.  Launched as a
 // programmatic dependent of the streaming kernel: it may be scheduled while
 // that kernel drains and waits for its completion before reading.  The
 // partials are dead once read: with a 128-byte-aligned workspace their L2
@@ -22,6 +30,19 @@ namespace {
 constexpr int kReduceThreads = 256;
 constexpr int kGroup = 8;   // partials loaded before they are summed
 
+// s + p = s' + e exactly (Knuth's TwoSum; no ordering of |s|, |p| needed).
+// Plain IEEE additions: nvcc never reassociates or contracts them.  A
+// non-finite sum keeps e = 0, so Inf stays Inf (not Inf - Inf = NaN) and NaN
+// stays NaN, as in the plain sum.
+__device__ __forceinline__ void two_sum(float& s, float& e_acc, float p) {
+    const float t = s + p;
+    const float pp = t - s;
+    const float e = (s - (t - pp)) + (p - pp);
+    s = t;
+    e_acc += isfinite(t) ? e : 0.f;
+}
+
+template <bool COMP>
 __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4* __restrict__ part,
                                                                    float4* __restrict__ dw, int S,
                                                                    int64_t n4, int discard) {
@@ -29,6 +50,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
     const int64_t i = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x;
     const bool valid = i < n4;   // n4 % 8 == 0: a 128-byte line is all valid or all not
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 c = make_float4(0.f, 0.f, 0.f, 0.f);   // compensation (COMP only)
     for (int s0 = 0; valid && s0 < S; s0 += kGroup) {
         float4 b[kGroup];
 #pragma unroll
@@ -39,11 +61,19 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
             if (s0 + g < S) {
                 if (s0 + g == 0) {
                     a = b[g];
+                } else if (COMP) {
+                    two_sum(a.x, c.x, b[g].x);
+                    two_sum(a.y, c.y, b[g].y);
+                    two_sum(a.z, c.z, b[g].z);
+                    two_sum(a.w, c.w, b[g].w);
                 } else {
                     a.x += b[g].x; a.y += b[g].y; a.z += b[g].z; a.w += b[g].w;
                 }
             }
         }
+    }
+    if (COMP) {
+        a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
     }
     if (valid) dw[i] = a;
     // Every lane of a 128-byte line (8 float4) has consumed its loads once the
@@ -56,7 +86,8 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
 
 }  // namespace
 
-cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, cudaStream_t stream) {
+cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, bool compensated,
+                          cudaStream_t stream) {
     const int64_t n4 = n / 4;
     // discard needs 128-byte-aligned lines: every s-slice starts at a multiple
     // of 96 K bytes (K % 8 == 0, so a multiple of 768) from the base
@@ -71,8 +102,10 @@ cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, cud
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, reduce_dw_kernel, reinterpret_cast<const float4*>(partial),
-                              reinterpret_cast<float4*>(dw), S, n4, discard);
+    const float4* part4 = reinterpret_cast<const float4*>(partial);
+    float4* dw4 = reinterpret_cast<float4*>(dw);
+    if (compensated) return cudaLaunchKernelEx(&cfg, reduce_dw_kernel<true>, part4, dw4, S, n4, discard);
+    return cudaLaunchKernelEx(&cfg, reduce_dw_kernel<false>, part4, dw4, S, n4, discard);
 }
 
 }  // namespace mhcpb

@@ -123,6 +123,32 @@ def make(name: str, T: int, K: int, seed: int, *, addend: bool = False,
     )
 
 
+def make_dw_cancellation(K: int, seed: int, chunk: int = 512) -> Workload:
+    """Three chunks of ``chunk`` tokens whose dW contributions are 2**24, 1 and
+    1 for every (j, k): X is zero except X[0, :] = 2**24, X[chunk, :] = 1 and
+    X[2 * chunk, :] = 1 (all exact in BF16), grad_proj[:, :24] is zero except
+    1.0 on those three rows, grad_r = 0.  Every product and every per-chunk
+    sum is exact, and the exact dW = 2**24 + 2 is an FP32 value, but adding
+    the three chunk sums one FP32 rounding at a time gives 2**24 (2**24 + 1 is
+    a tie that rounds to even).  W is drawn from ``seed``."""
+    T = 3 * chunk
+    g = torch.Generator().manual_seed(seed)
+    w = torch.randn(N_PROJ, K, generator=g, dtype=torch.float32) * 0.02
+    x = torch.zeros(T, K, dtype=torch.float32)
+    x[0, :] = 2.0 ** 24
+    x[chunk, :] = 1.0
+    x[2 * chunk, :] = 1.0
+    gp = torch.zeros(T, GRAD_PROJ_COLS, dtype=torch.float32)
+    gp[[0, chunk, 2 * chunk], :N_PROJ] = 1.0
+    x_bits = _bf16_bits(x)
+    return Workload(
+        name="dw_cancellation", T=T, K=K, seed=seed, x=x_bits,
+        w=w.numpy().astype(np.float32, copy=False),
+        grad_proj=gp.numpy(), grad_r=np.zeros(T, dtype=np.float32), r=rms_from_x(x_bits),
+        notes={"exact_dw": float(2 ** 24 + 2)},
+    )
+
+
 # The five named workloads: (T, K, seed, addend, edge).  K = n_streams * hidden.
 CONFIGS = {
     "tiny": dict(T=64, K=4 * 128, seed=0),

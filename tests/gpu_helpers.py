@@ -29,9 +29,10 @@ def to_dev(wl):
 class Runner:
     """A plan plus output/workspace buffers for one workload shape."""
 
-    def __init__(self, wl, fma_kernel=False, fill=float("nan")):
+    def __init__(self, wl, fma_kernel=False, fill=float("nan"), compensated_dw=False):
         self.wl = wl
-        self.plan = Plan(wl.T, wl.K, 0, addend=wl.has_addend, fma_kernel=fma_kernel)
+        self.plan = Plan(wl.T, wl.K, 0, addend=wl.has_addend, fma_kernel=fma_kernel,
+                         compensated_dw=compensated_dw)
         self.inp = to_dev(wl)
         self.dx = torch.full((wl.T, wl.K), fill, dtype=torch.bfloat16, device=DEV)
         self.dw = torch.full((24, wl.K), fill, dtype=torch.float32, device=DEV)
@@ -50,8 +51,8 @@ class Runner:
         return dx, dw
 
 
-def run_gpu(wl, fma_kernel=False):
-    r = Runner(wl, fma_kernel=fma_kernel)
+def run_gpu(wl, fma_kernel=False, compensated_dw=False):
+    r = Runner(wl, fma_kernel=fma_kernel, compensated_dw=compensated_dw)
     r.run()
     out = r.results()
     r.plan.close()

@@ -200,6 +200,27 @@ def test_p_zero_gives_rms_term_only_and_zero_dw():
             assert int(dx[t, k]) == int(O.bf16_rne_from_f64(np.array([c * X[t, k]]))[0])
 
 
+def test_dw_cancellation_case_closed_form():
+    """The input behind the compensated-reduction pin: the oracle's dW is
+    exactly 2**24 + 2 (an FP32 value), its per-chunk sums are exactly 2**24, 1
+    and 1, and adding those one FP32 rounding at a time gives 2**24 instead:
+    the case separates a once-rounded sum from a sequential FP32 one."""
+    wl = WL.make_dw_cancellation(K=16, seed=5)
+    dw = O.dw_f64(wl.x, wl.grad_proj)
+    assert np.all(dw == 2.0 ** 24 + 2)
+    assert np.all(dw.astype(np.float32) == np.float32(16777218.0))
+    chunks = [O.dw_f64(wl.x[s * 512:(s + 1) * 512], wl.grad_proj[s * 512:(s + 1) * 512])
+              for s in range(3)]
+    assert [float(c[0, 0]) for c in chunks] == [2.0 ** 24, 1.0, 1.0]
+    seq = np.float32(chunks[0][0, 0])
+    for c in chunks[1:]:
+        seq = np.float32(seq + np.float32(c[0, 0]))
+    assert seq == np.float32(2.0 ** 24)
+    # dX is the plain product (grad_r = 0): bf16(P @ W) on the three rows, 0 elsewhere
+    dx, _ = O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
+    assert np.all(dx[1:512] == 0) and np.any(dx[0] != 0)
+
+
 def test_ignored_grad_proj_columns():
     wl = WL.make("t", T=19, K=32, seed=23)
     ref = O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)

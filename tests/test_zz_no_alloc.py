@@ -113,3 +113,18 @@ def test_static_scratch_matches_workspace_entry_point_twice():
         okw, stw = O.check_dw(got_dw, ref_dw.astype(np.float64), O.dw_abs_bound(wl.x, wl.grad_proj))
         assert okw, f"T={wl.T} K={wl.K}: dW differs from mhcpb_execute: {stw}"
         del d
+
+
+@pytest.mark.gpu
+def test_static_scratch_compensated_dw_once_rounded():
+    """MHCPB_COMPENSATED_DW through the allocation-free entry point: the
+    cancellation input's exact dW, 2**24 + 2, comes back bit for bit."""
+    wl = WL.make_dw_cancellation(K=256, seed=52)
+    d = _dev(wl)
+    dx, dw = _outputs(wl)
+    abi.mhcpb_execute_static_scratch(
+        wl.T, wl.K, abi.MHCPB_ALLOW_TF32 | abi.MHCPB_COMPENSATED_DW, d["x"].data_ptr(),
+        d["w"].data_ptr(), d["gp"].data_ptr(), d["gr"].data_ptr(), d["r"].data_ptr(),
+        dx.data_ptr(), dw.data_ptr(), None, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert np.all(dw.cpu().numpy() == np.float32(16777218.0))
