@@ -102,6 +102,14 @@ enum {
      * FP32 once; here it is applied to the cross-chunk reduction.  Costs a
      * few FP32 operations per partial in the second kernel only. */
     MHCPB_COMPENSATED_DW = 8u,
+    /* Accumulate dW into the caller's buffer instead of overwriting it:
+     * dW_out = dW_in + D in FP32 (one rounding), where D is exactly what the
+     * execute would write without this flag (plain or compensated).  For
+     * callers that sum weight gradients over micro-batches in an FP32 buffer of
+     * their own (the pages' "accumulate FP8 weight gradients straight into a
+     * caller's fp32 buffer", prime-kernels PR #15, applied here to dW).  dW must
+     * then hold valid values before the execute; dX is unaffected. */
+    MHCPB_ACCUMULATE_DW = 16u,
     /* Test hook for failure detection: in the tensor-core kernel the MMA
      * issuer first waits on a barrier that nothing completes, so the execute
      * ends by the in-kernel wait limit, records MHCPB_ERR_DEVICE_TIMEOUT in the
@@ -147,6 +155,29 @@ mhcpb_status_t mhcpb_execute(mhcpb_plan_t plan,
                              void* dx, float* dw,
                              void* workspace, size_t workspace_bytes,
                              const void* grad_x_addend, void* stream);
+
+/* The same backward in two calls, so that a caller can start using dX (send
+ * it, or run the next layer's backward) before dW exists -- the split
+ * backward of the prime-kernels PR #15 ("data gradient first, weight
+ * gradients after"), applied to this stage:
+ *
+ *   mhcpb_execute_dx: enqueues the streaming kernel only.  When it completes,
+ *   dX is final and `workspace` holds the dW partials of these inputs.
+ *   mhcpb_reduce_dw:  enqueues the reduction only: dW from the partials that
+ *   the last mhcpb_execute_dx with this workspace left there (overwritten, or
+ *   accumulated with MHCPB_ACCUMULATE_DW).
+ *
+ * Arguments, checks and status codes are those of mhcpb_execute for the
+ * operands each call uses.  The caller orders the two (same stream, or an
+ * event) and must not touch the workspace in between.  dX and dW are
+ * bitwise identical to mhcpb_execute's. */
+mhcpb_status_t mhcpb_execute_dx(mhcpb_plan_t plan,
+                                const void* x, const float* w, const float* grad_proj,
+                                const float* grad_r, const float* r, void* dx,
+                                void* workspace, size_t workspace_bytes,
+                                const void* grad_x_addend, void* stream);
+mhcpb_status_t mhcpb_reduce_dw(mhcpb_plan_t plan, void* workspace, size_t workspace_bytes,
+                               float* dw, void* stream);
 
 /* mhcpb_execute with timing events for measurement tools: records
  * `ev_before` (a cudaEvent_t, may be NULL) before the streaming kernel,
@@ -208,8 +239,8 @@ mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas);
  *  - Runs on the calling thread's current device; all pointers must be device
  *    memory there, 16-byte aligned and disjoint (same contract and status codes
  *    as mhcpb_execute).  `flags` must contain MHCPB_ALLOW_TF32 and may contain
- *    MHCPB_HAS_ADDEND (then `grad_x_addend` is required) and
- *    MHCPB_COMPENSATED_DW, nothing else.
+ *    MHCPB_HAS_ADDEND (then `grad_x_addend` is required), MHCPB_COMPENSATED_DW
+ *    and MHCPB_ACCUMULATE_DW, nothing else.
  *  - The first call on a device does that device's set-up (looks up the
  *    buffer's device address, raises the kernels' shared-memory limit).  Make
  *    that first call before any stream capture.

@@ -14,8 +14,8 @@ from __future__ import annotations
 
 from . import abi
 from .abi import (  # noqa: F401
-    MHCPB_ALLOW_TF32, MHCPB_COMPENSATED_DW, MHCPB_FMA_KERNEL, MHCPB_HAS_ADDEND, MhcpbError,
-    mhcpb_destroy,
+    MHCPB_ACCUMULATE_DW, MHCPB_ALLOW_TF32, MHCPB_COMPENSATED_DW, MHCPB_FMA_KERNEL,
+    MHCPB_HAS_ADDEND, MhcpbError, mhcpb_destroy, mhcpb_execute_dx, mhcpb_reduce_dw,
     mhcpb_execute, mhcpb_get_device_status, mhcpb_last_cuda_error, mhcpb_plan_create,
     mhcpb_plan_query, mhcpb_plan_set_max_ctas, mhcpb_plan_set_wait_limit, mhcpb_status_string,
     mhcpb_workspace_bytes,
@@ -27,10 +27,12 @@ class Plan:
 
     def __init__(self, T: int, K: int, device: int = 0, *, addend: bool = False,
                  fma_kernel: bool = False, compensated_dw: bool = False,
-                 test_inject_stall: bool = False):
+                 accumulate_dw: bool = False, test_inject_stall: bool = False):
         flags = abi.MHCPB_ALLOW_TF32
         if compensated_dw:
             flags |= abi.MHCPB_COMPENSATED_DW
+        if accumulate_dw:
+            flags |= abi.MHCPB_ACCUMULATE_DW
         if test_inject_stall:
             flags |= abi.MHCPB_TEST_INJECT_STALL
         if addend:
@@ -62,6 +64,26 @@ class Plan:
                       grad_r.data_ptr(), r.data_ptr(), dx.data_ptr(), dw.data_ptr(),
                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                       None if addend is None else addend.data_ptr(), stream)
+
+    @staticmethod
+    def _stream(stream, like):
+        if stream is None:
+            import torch
+            return torch.cuda.current_stream(like.device).cuda_stream
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+    def execute_dx(self, x, w, grad_proj, grad_r, r, dx, workspace, addend=None, stream=None):
+        """First half of the split backward: dX, and the dW partials in
+        ``workspace`` (see ``mhcpb_execute_dx``)."""
+        mhcpb_execute_dx(self.handle, x.data_ptr(), w.data_ptr(), grad_proj.data_ptr(),
+                         grad_r.data_ptr(), r.data_ptr(), dx.data_ptr(), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(),
+                         None if addend is None else addend.data_ptr(), self._stream(stream, x))
+
+    def reduce_dw(self, workspace, dw, stream=None):
+        """Second half: dW from the partials in ``workspace``."""
+        mhcpb_reduce_dw(self.handle, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        dw.data_ptr(), self._stream(stream, dw))
 
     def device_status(self, clear: bool = False) -> int:
         return mhcpb_get_device_status(self.handle, clear)

@@ -30,6 +30,7 @@ MHCPB_ALLOW_TF32 = 1
 MHCPB_HAS_ADDEND = 2
 MHCPB_FMA_KERNEL = 4
 MHCPB_COMPENSATED_DW = 8
+MHCPB_ACCUMULATE_DW = 16
 MHCPB_TEST_INJECT_STALL = 1 << 30
 
 MHCPB_NPROJ = 24
@@ -46,7 +47,8 @@ QUERY = {"T": 0, "K": 1, "S": 2, "grid": 3, "flags": 4, "smem": 5, "token_tile":
 EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcpb_execute_profiled",
             "mhcpb_get_device_status", "mhcpb_plan_query", "mhcpb_plan_set_wait_limit",
             "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error",
-            "mhcpb_execute_static_scratch", "mhcpb_plan_set_max_ctas")
+            "mhcpb_execute_static_scratch", "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx",
+            "mhcpb_reduce_dw")
 
 
 class MhcpbError(RuntimeError):
@@ -81,6 +83,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_plan_set_wait_limit.argtypes = [P, ctypes.c_uint64]
     lib.mhcpb_plan_set_max_ctas.argtypes = [P, I32]
     lib.mhcpb_execute_static_scratch.argtypes = [I64, I64, U32, P, P, P, P, P, P, P, P, P]
+    lib.mhcpb_execute_dx.argtypes = [P, P, P, P, P, P, P, P, SZ, P, P]
+    lib.mhcpb_reduce_dw.argtypes = [P, P, SZ, P, P]
     lib.mhcpb_destroy.argtypes = [P]
     lib.mhcpb_status_string.argtypes = [I32]
     lib.mhcpb_status_string.restype = ctypes.c_char_p
@@ -89,7 +93,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute",
                  "mhcpb_execute_profiled", "mhcpb_get_device_status", "mhcpb_plan_query",
                  "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch",
-                 "mhcpb_plan_set_max_ctas"):
+                 "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx", "mhcpb_reduce_dw"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -124,6 +128,20 @@ def mhcpb_execute(plan: int, x: int, w: int, grad_proj: int, grad_r: int, r: int
     _check(load().mhcpb_execute(plan, x, w, grad_proj, grad_r, r, dx, dw, workspace,
                                 int(workspace_bytes), grad_x_addend or None, stream or None),
            "mhcpb_execute")
+
+
+def mhcpb_execute_dx(plan: int, x: int, w: int, grad_proj: int, grad_r: int, r: int, dx: int,
+                     workspace: int, workspace_bytes: int, grad_x_addend: int | None,
+                     stream: int | None) -> None:
+    _check(load().mhcpb_execute_dx(plan, x, w, grad_proj, grad_r, r, dx, workspace,
+                                   int(workspace_bytes), grad_x_addend or None, stream or None),
+           "mhcpb_execute_dx")
+
+
+def mhcpb_reduce_dw(plan: int, workspace: int, workspace_bytes: int, dw: int,
+                    stream: int | None) -> None:
+    _check(load().mhcpb_reduce_dw(plan, workspace, int(workspace_bytes), dw, stream or None),
+           "mhcpb_reduce_dw")
 
 
 def mhcpb_get_device_status(plan: int, clear: bool = False) -> int:

@@ -187,7 +187,8 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
     if (out == nullptr) return MHCPB_ERR_INVALID_ARG;
     if ((flags & MHCPB_ALLOW_TF32) == 0) return MHCPB_ERR_TF32_NOT_ALLOWED;
     if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND | MHCPB_FMA_KERNEL |
-                            MHCPB_COMPENSATED_DW | MHCPB_TEST_INJECT_STALL)) != 0)
+                            MHCPB_COMPENSATED_DW | MHCPB_ACCUMULATE_DW |
+                            MHCPB_TEST_INJECT_STALL)) != 0)
         return MHCPB_ERR_INVALID_ARG;
     if (T < 1 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
         return MHCPB_ERR_UNSUPPORTED_SHAPE;
@@ -296,24 +297,42 @@ mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value) {
     return MHCPB_OK;
 }
 
-static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float* w,
+// What an execute enqueues: kernel 1 (dX and the dW partials), kernel 2 (the
+// fixed-order reduction of the partials into dW), or both.
+enum : int { kRunStream = 1, kRunReduce = 2, kRunBoth = 3 };
+
+static mhcpb_status_t execute_impl(mhcpb_plan_t plan, int what, const void* x, const float* w,
                                    const float* grad_proj, const float* grad_r, const float* r,
                                    void* dx, float* dw, void* workspace, size_t workspace_bytes,
                                    const void* grad_x_addend, void* stream, void* ev0, void* ev1,
                                    void* ev2) {
     if (plan == nullptr) return MHCPB_ERR_INVALID_ARG;
+    const bool run1 = (what & kRunStream) != 0, run2 = (what & kRunReduce) != 0;
     const bool add = (plan->flags & MHCPB_HAS_ADDEND) != 0;
-    if (!x || !w || !grad_proj || !grad_r || !r || !dx || !dw || !workspace)
-        return MHCPB_ERR_INVALID_ARG;
-    if (add != (grad_x_addend != nullptr)) return MHCPB_ERR_INVALID_ARG;
+    if (!workspace) return MHCPB_ERR_INVALID_ARG;
+    if (run1 && (!x || !w || !grad_proj || !grad_r || !r || !dx)) return MHCPB_ERR_INVALID_ARG;
+    if (run1 && add != (grad_x_addend != nullptr)) return MHCPB_ERR_INVALID_ARG;
+    if (run2 && !dw) return MHCPB_ERR_INVALID_ARG;
     if (workspace_bytes < plan->ws_bytes) return MHCPB_ERR_WORKSPACE_TOO_SMALL;
 
     const int64_t T = plan->T, K = plan->K;
-    const void* ptrs[9] = {x, w, grad_proj, grad_r, r, dx, dw, workspace, grad_x_addend};
-    const size_t sizes[9] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4), (size_t)(T * kGradProjCols * 4),
-                             (size_t)(T * 4), (size_t)(T * 4), (size_t)(T * K * 2),
-                             (size_t)(kNProj * K * 4), plan->ws_bytes, (size_t)(T * K * 2)};
-    const int n = add ? 9 : 8;
+    // operands of the kernels that run: 0..5 kernel 1's inputs and dX, 6 dW,
+    // 7 the workspace, 8 the addend
+    const void* all[9] = {x, w, grad_proj, grad_r, r, dx, dw, workspace, grad_x_addend};
+    const size_t all_sizes[9] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4),
+                                 (size_t)(T * kGradProjCols * 4), (size_t)(T * 4), (size_t)(T * 4),
+                                 (size_t)(T * K * 2), (size_t)(kNProj * K * 4), plan->ws_bytes,
+                                 (size_t)(T * K * 2)};
+    const void* ptrs[9];
+    size_t sizes[9];
+    int n = 0;
+    for (int i = 0; i < 9; ++i) {
+        const bool used = (i <= 5) ? run1 : (i == 6) ? run2 : (i == 7) ? true : (run1 && add);
+        if (used) {
+            ptrs[n] = all[i];
+            sizes[n++] = all_sizes[i];
+        }
+    }
     for (int i = 0; i < n; ++i)
         if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != 0) return MHCPB_ERR_MISALIGNED;
     Range rg[9];
@@ -333,45 +352,49 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, const void* x, const float
     if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-    MainParams p{};
-    p.T = (int32_t)T;
-    p.K = (int32_t)K;
-    p.S = plan->S;
-    p.chunk = plan->chunk;
-    p.n_strips = plan->n_strips;
-    p.half_units = plan->half_units;
-    p.x = static_cast<const uint16_t*>(x);
-    p.w = w;
-    p.grad_proj = grad_proj;
-    p.grad_r = grad_r;
-    p.r = r;
-    p.dx = static_cast<uint16_t*>(dx);
-    p.addend = static_cast<const uint16_t*>(grad_x_addend);
-    p.partial = static_cast<float*>(workspace);
-    p.status = plan->d_status;
-    p.timeout_ns = plan->timeout_ns;
-    p.test_flags = (plan->flags & MHCPB_TEST_INJECT_STALL) ? kTestInjectStall : 0u;
-    p.trace = plan->d_trace;
-
     cudaError_t e;
     if (ev0 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev0), st)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord");
-    if (plan->flags & MHCPB_FMA_KERNEL) {
-        e = fma::launch(p, st);
-        if (e != cudaSuccess) return cuda_fail(e, "launch (FMA kernel)");
-    } else {
-        CUtensorMap m[6];
-        if (const char* bad = encode_maps(m, T, K, x, dx, add ? grad_x_addend : x, grad_proj,
-                                          grad_r, r))
-            return cuda_fail(cudaErrorInvalidValue, bad);
-        e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], plan->grid, plan->epi_warps, st);
-        if (e != cudaSuccess) return cuda_fail(e, "launch (tensor-core kernel)");
+    if (run1) {
+        MainParams p{};
+        p.T = (int32_t)T;
+        p.K = (int32_t)K;
+        p.S = plan->S;
+        p.chunk = plan->chunk;
+        p.n_strips = plan->n_strips;
+        p.half_units = plan->half_units;
+        p.x = static_cast<const uint16_t*>(x);
+        p.w = w;
+        p.grad_proj = grad_proj;
+        p.grad_r = grad_r;
+        p.r = r;
+        p.dx = static_cast<uint16_t*>(dx);
+        p.addend = static_cast<const uint16_t*>(grad_x_addend);
+        p.partial = static_cast<float*>(workspace);
+        p.status = plan->d_status;
+        p.timeout_ns = plan->timeout_ns;
+        p.test_flags = (plan->flags & MHCPB_TEST_INJECT_STALL) ? kTestInjectStall : 0u;
+        p.trace = plan->d_trace;
+        if (plan->flags & MHCPB_FMA_KERNEL) {
+            e = fma::launch(p, st);
+            if (e != cudaSuccess) return cuda_fail(e, "launch (FMA kernel)");
+        } else {
+            CUtensorMap m[6];
+            if (const char* bad = encode_maps(m, T, K, x, dx, add ? grad_x_addend : x, grad_proj,
+                                              grad_r, r))
+                return cuda_fail(cudaErrorInvalidValue, bad);
+            e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], plan->grid, plan->epi_warps, st);
+            if (e != cudaSuccess) return cuda_fail(e, "launch (tensor-core kernel)");
+        }
     }
     if (ev1 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev1), st)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord");
-    e = launch_reduce(p.partial, dw, plan->S, (int64_t)kNProj * K,
-                      (plan->flags & MHCPB_COMPENSATED_DW) != 0, st);
-    if (e != cudaSuccess) return cuda_fail(e, "launch (dW reduction)");
+    if (run2) {
+        e = launch_reduce(static_cast<const float*>(workspace), dw, plan->S, (int64_t)kNProj * K,
+                          (plan->flags & MHCPB_COMPENSATED_DW) != 0,
+                          (plan->flags & MHCPB_ACCUMULATE_DW) != 0, st);
+        if (e != cudaSuccess) return cuda_fail(e, "launch (dW reduction)");
+    }
     if (ev2 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev2), st)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord");
     return MHCPB_OK;
@@ -381,8 +404,8 @@ mhcpb_status_t mhcpb_execute(mhcpb_plan_t plan, const void* x, const float* w,
                              const float* grad_proj, const float* grad_r, const float* r, void* dx,
                              float* dw, void* workspace, size_t workspace_bytes,
                              const void* grad_x_addend, void* stream) {
-    return execute_impl(plan, x, w, grad_proj, grad_r, r, dx, dw, workspace, workspace_bytes,
-                        grad_x_addend, stream, nullptr, nullptr, nullptr);
+    return execute_impl(plan, kRunBoth, x, w, grad_proj, grad_r, r, dx, dw, workspace,
+                        workspace_bytes, grad_x_addend, stream, nullptr, nullptr, nullptr);
 }
 
 mhcpb_status_t mhcpb_execute_profiled(mhcpb_plan_t plan, const void* x, const float* w,
@@ -390,8 +413,22 @@ mhcpb_status_t mhcpb_execute_profiled(mhcpb_plan_t plan, const void* x, const fl
                                       void* dx, float* dw, void* workspace, size_t workspace_bytes,
                                       const void* grad_x_addend, void* stream, void* ev_before,
                                       void* ev_between, void* ev_after) {
-    return execute_impl(plan, x, w, grad_proj, grad_r, r, dx, dw, workspace, workspace_bytes,
-                        grad_x_addend, stream, ev_before, ev_between, ev_after);
+    return execute_impl(plan, kRunBoth, x, w, grad_proj, grad_r, r, dx, dw, workspace,
+                        workspace_bytes, grad_x_addend, stream, ev_before, ev_between, ev_after);
+}
+
+mhcpb_status_t mhcpb_execute_dx(mhcpb_plan_t plan, const void* x, const float* w,
+                                const float* grad_proj, const float* grad_r, const float* r,
+                                void* dx, void* workspace, size_t workspace_bytes,
+                                const void* grad_x_addend, void* stream) {
+    return execute_impl(plan, kRunStream, x, w, grad_proj, grad_r, r, dx, nullptr, workspace,
+                        workspace_bytes, grad_x_addend, stream, nullptr, nullptr, nullptr);
+}
+
+mhcpb_status_t mhcpb_reduce_dw(mhcpb_plan_t plan, void* workspace, size_t workspace_bytes,
+                               float* dw, void* stream) {
+    return execute_impl(plan, kRunReduce, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dw,
+                        workspace, workspace_bytes, nullptr, stream, nullptr, nullptr, nullptr);
 }
 
 mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status, int clear) {

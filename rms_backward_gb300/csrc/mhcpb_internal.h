@@ -42,7 +42,7 @@ struct MainParams {
 };
 
 // Timeline stamps of a traced build: [grid][kTraceEvents][kTraceTiles] u64.
-constexpr int kTraceEvents = 16;
+constexpr int kTraceEvents = 19;
 constexpr int kTraceTiles = 48;
 
 constexpr uint32_t kTestInjectStall = 1u;
@@ -91,8 +91,9 @@ const char* encode_tc_maps(CUtensorMap (&m)[6], int64_t T, int64_t K, const void
 int record_cuda_error(cudaError_t e, const char* what);
 
 // Second kernel: dW[j,k] = sum over s ascending of partial[s][j][k]; with
-// `compensated`, TwoSum at every addition and one final rounding.
+// `compensated`, TwoSum at every addition and one final rounding; with
+// `accumulate`, the result is added to dW's previous contents.
 cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, bool compensated,
-                          cudaStream_t stream);
+                          bool accumulate, cudaStream_t stream);
 
 }  // namespace mhcpb

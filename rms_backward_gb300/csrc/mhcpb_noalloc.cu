@@ -87,7 +87,8 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
                                                        void* dx, float* dw,
                                                        const void* grad_x_addend, void* stream) {
     if ((flags & MHCPB_ALLOW_TF32) == 0) return MHCPB_ERR_TF32_NOT_ALLOWED;
-    if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND | MHCPB_COMPENSATED_DW)) != 0)
+    if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND | MHCPB_COMPENSATED_DW |
+                             MHCPB_ACCUMULATE_DW)) != 0)
         return MHCPB_ERR_INVALID_ARG;
     if (T < 1 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
         return MHCPB_ERR_UNSUPPORTED_SHAPE;
@@ -151,7 +152,8 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
     if ((e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], grid, kEpiWarps, st)) != cudaSuccess)
         return (mhcpb_status_t)record_cuda_error(e, "launch (tensor-core kernel)");
     if ((e = launch_reduce(p.partial, dw, p.S, (int64_t)kNProj * K,
-                           (flags & MHCPB_COMPENSATED_DW) != 0, st)) != cudaSuccess)
+                           (flags & MHCPB_COMPENSATED_DW) != 0,
+                           (flags & MHCPB_ACCUMULATE_DW) != 0, st)) != cudaSuccess)
         return (mhcpb_status_t)record_cuda_error(e, "launch (dW reduction)");
     return MHCPB_OK;
 }

@@ -9,6 +9,10 @@
 // One thread owns four consecutive dW elements; the sum runs over s in
 // ascending order, so dW depends only on (T, K) and the inputs.
 //
+// With the plan flag MHCPB_ACCUMULATE_DW the result is added to the dW the
+// caller passes (dW_out = dW_in + result, one FP32 addition) instead of
+// overwriting it.
+//
 // Compensated variant (plan flag MHCPB_COMPENSATED_DW): the same order, with
 // Knuth's TwoSum at every addition, s + p = s' + e exactly (six FP32
 // additions, no branch), the errors e summed beside s and added once at the
@@ -42,7 +46,7 @@ __device__ __forceinline__ void two_sum(float& s, float& e_acc, float p) {
     e_acc += isfinite(t) ? e : 0.f;
 }
 
-template <bool COMP>
+template <bool COMP, bool ACC>
 __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4* __restrict__ part,
                                                                    float4* __restrict__ dw, int S,
                                                                    int64_t n4, int discard) {
@@ -75,7 +79,13 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
     if (COMP) {
         a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
     }
-    if (valid) dw[i] = a;
+    if (valid) {
+        if (ACC) {   // accumulate into the caller's dW: one more FP32 rounding
+            const float4 o = dw[i];
+            a.x = o.x + a.x; a.y = o.y + a.y; a.z = o.z + a.z; a.w = o.w + a.w;
+        }
+        dw[i] = a;
+    }
     // Every lane of a 128-byte line (8 float4) has consumed its loads once the
     // warp has converged here; then one lane per line drops the line.
     __syncwarp();
@@ -87,7 +97,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
 }  // namespace
 
 cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, bool compensated,
-                          cudaStream_t stream) {
+                          bool accumulate, cudaStream_t stream) {
     const int64_t n4 = n / 4;
     // discard needs 128-byte-aligned lines: every s-slice starts at a multiple
     // of 96 K bytes (K % 8 == 0, so a multiple of 768) from the base
@@ -104,8 +114,11 @@ cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, boo
     cfg.numAttrs = 1;
     const float4* part4 = reinterpret_cast<const float4*>(partial);
     float4* dw4 = reinterpret_cast<float4*>(dw);
-    if (compensated) return cudaLaunchKernelEx(&cfg, reduce_dw_kernel<true>, part4, dw4, S, n4, discard);
-    return cudaLaunchKernelEx(&cfg, reduce_dw_kernel<false>, part4, dw4, S, n4, discard);
+    if (compensated)
+        return accumulate ? cudaLaunchKernelEx(&cfg, reduce_dw_kernel<true, true>, part4, dw4, S, n4, discard)
+                          : cudaLaunchKernelEx(&cfg, reduce_dw_kernel<true, false>, part4, dw4, S, n4, discard);
+    return accumulate ? cudaLaunchKernelEx(&cfg, reduce_dw_kernel<false, true>, part4, dw4, S, n4, discard)
+                      : cudaLaunchKernelEx(&cfg, reduce_dw_kernel<false, false>, part4, dw4, S, n4, discard);
 }
 
 }  // namespace mhcpb

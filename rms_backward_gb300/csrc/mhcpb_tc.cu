@@ -121,15 +121,28 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile ui
             p.trace[((size_t)blockIdx.x * kTraceEvents + (ev)) * kTraceTiles + (n)] =      \
                 ptx::globaltimer();                                                         \
     } while (0)
+// the latest of several warps' stamps for one event, with the warp index in
+// the low 3 bits (stamp << 3 | warp & 7)
+#define TRACE_MAX(ev, n)                                                                    \
+    do {                                                                                    \
+        if (p.trace != nullptr && (n) < kTraceTiles)                                       \
+            atomicMax(reinterpret_cast<unsigned long long*>(                               \
+                          &p.trace[((size_t)blockIdx.x * kTraceEvents + (ev)) * kTraceTiles + (n)]), \
+                      ((unsigned long long)ptx::globaltimer() << 3) | (unsigned long long)(warp & 7)); \
+    } while (0)
 #else
 #define TRACE(ev, n) \
     do {             \
+    } while (0)
+#define TRACE_MAX(ev, n) \
+    do {                 \
     } while (0)
 #endif
 enum TraceEvent {
     EV_PROD_ISSUE = 0, EV_MMA_XFULL, EV_MMA_PFULL, EV_MMA_ACCEMPTY, EV_MMA_ISSUED, EV_EPI_ACCFULL,
     EV_EPI_STORED, EV_EPI_RELEASE, EV_PREP_XFULL, EV_PREP_PEMPTY, EV_PREP_DONE, EV_PROD_XEMPTY,
-    EV_CTA_START, EV_CTA_END, EV_DRAIN_START, EV_DRAIN_END   // drains indexed by item
+    EV_CTA_START, EV_CTA_END, EV_DRAIN_START, EV_DRAIN_END,   // drains indexed by item
+    EV_EPI_ACCFULL_LAST, EV_EPI_STORED_LAST, EV_EPI_RELEASE_LAST   // latest epilogue warp
 };
 
 __device__ __forceinline__ float tf32_rna(float v) {
@@ -628,6 +641,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     break;
                 }
                 if (e == 0 && lane == 0) TRACE(EV_EPI_ACCFULL, n);
+                if (lane == 0) TRACE_MAX(EV_EPI_ACCFULL_LAST, n);
                 ptx::tc_fence_after();
                 if (last) {
                     // the MMAs whose completion ACC_FULL signalled include the item's
@@ -712,9 +726,11 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 if (lane == 0) {
                     ptx::bulk_commit();
                     if (e == 0) TRACE(EV_EPI_STORED, n);
+                    TRACE_MAX(EV_EPI_STORED_LAST, n);
                     ptx::bulk_wait_read<0>();          // this tile's stores have read smem
                     ptx::mbar_arrive(bar(C::B_XE + xs));
                     if (e == 0) TRACE(EV_EPI_RELEASE, n);
+                    TRACE_MAX(EV_EPI_RELEASE_LAST, n);
                 }
                 __syncwarp();
                 if (++xs == NS) { xs = 0; xph ^= 1u; }
@@ -722,7 +738,10 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                 if (last) store_partial();
             }
         }
-        if (lane == 0) ptx::bulk_wait<0>();   // all dX stores of this warp are complete
+        // every dX store of this warp has read its shared memory (each tile
+        // waited for that before releasing its stage); their global writes
+        // complete with the grid, so the CTA need not wait for them
+        if (lane == 0) ptx::bulk_wait_read<0>();
         __syncwarp();
     }
 

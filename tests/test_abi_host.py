@@ -74,6 +74,8 @@ def test_null_arguments_rejected(lib):
     assert lib.mhcpb_plan_create(None, 10, 16, 0, 1) == abi.MHCPB_ERR_INVALID_ARG
     assert lib.mhcpb_workspace_bytes(None, None) == abi.MHCPB_ERR_INVALID_ARG
     assert lib.mhcpb_execute(None, *([None] * 8), 0, None, None) == abi.MHCPB_ERR_INVALID_ARG
+    assert lib.mhcpb_execute_dx(None, *([None] * 7), 0, None, None) == abi.MHCPB_ERR_INVALID_ARG
+    assert lib.mhcpb_reduce_dw(None, None, 0, None, None) == abi.MHCPB_ERR_INVALID_ARG
     assert lib.mhcpb_plan_query(None, 0, None) == abi.MHCPB_ERR_INVALID_ARG
     assert lib.mhcpb_destroy(None) == abi.MHCPB_OK
     v = ctypes.c_int()
