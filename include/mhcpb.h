@@ -209,11 +209,13 @@ mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value);
  * enqueued after the call. */
 mhcpb_status_t mhcpb_plan_set_wait_limit(mhcpb_plan_t plan, uint64_t nanoseconds);
 
-/* Caps the tensor-core kernel's persistent grid at `max_ctas` CTAs (one per
- * SM; 0 restores the default of every SM), e.g. to leave SMs to kernels that
- * run concurrently on other streams.  Results are bitwise identical for every
- * cap: the dW partition depends only on T.  No effect on MHCPB_FMA_KERNEL
- * plans.  Applies to executes enqueued after the call. */
+/* Caps the persistent grids of the tensor-core backward kernel and of the
+ * forward kernel at `max_ctas` CTAs (one per SM; 0 restores the default of
+ * every SM), e.g. to leave SMs to kernels that run concurrently on other
+ * streams.  Results are bitwise identical for every cap: the dW partition
+ * depends only on T, the forward's only on K.  The backward of
+ * MHCPB_FMA_KERNEL plans is not affected.  Applies to calls enqueued after
+ * this one. */
 mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas);
 
 /* Size of the library's built-in scratch buffer (see below): 16 MiB. */
@@ -255,6 +257,35 @@ mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uint32_t flags
                                             const float* grad_r, const float* r,
                                             void* dx, float* dw,
                                             const void* grad_x_addend, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The forward of the stage (SURVEY "next" row: the step before the backward).
+ * The prime-kernels PR #15 page describes its mhc_projection as the RMS of the
+ * streams and the projection logits in one read of the streams; this stage's
+ * backward (the cuDNN page above) receives the gradients of exactly these two
+ * outputs, and its dX formula is their vector-Jacobian product:
+ *
+ *     proj[t, j] = sum_k X[t, k] * W[j, k]      j < 24, TF32 W (nearest, ties
+ *                                                away), FP32 accumulation
+ *     r[t]       = sqrt(sum_k X[t, k]^2 / K + eps)
+ *
+ * Layouts: x BF16 [T, K] and w FP32 [24, K] as for the backward; proj FP32
+ * [T, 32] (overwritten; columns 24..31 written as zero, the layout the
+ * backward reads grad_proj in); r FP32 [T] (overwritten).  One streaming
+ * kernel (tensor cores for the projection, CUDA cores for the squares) and a
+ * fixed-order reduction of per-512-column partials: bitwise reproducible and
+ * independent of the SM count.  The stream collapse the page's forward also
+ * fuses needs weights the pages do not define and is not part of it.
+ *
+ * Uses the plan's T and K (any flags).  `eps` must be finite and >= 0.
+ * Workspace: mhcpb_forward_workspace_bytes (ceil(K/512) * 25 * T' * 4 bytes,
+ * T' = T rounded up to 32; 16,384,000 B at T=4096, K=20480), no
+ * initialisation needed.  Pointers 16-byte aligned, disjoint, on the plan's
+ * device; the same status codes and device status word as mhcpb_execute. */
+mhcpb_status_t mhcpb_forward_workspace_bytes(mhcpb_plan_t plan, size_t* bytes);
+mhcpb_status_t mhcpb_forward(mhcpb_plan_t plan, const void* x, const float* w, float eps,
+                             float* proj, float* r, void* workspace, size_t workspace_bytes,
+                             void* stream);
 
 /* Releases the plan (and its status word).  Safe on NULL. */
 mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan);

@@ -120,4 +120,5 @@ def check_r(r, ref, rel=2.0 ** -16):
     r = np.asarray(r, dtype=np.float64)
     err = np.abs(r - ref)
     bad = err > rel * ref
-    return (not bad.any()), dict(n=err.size, bad=int(bad.sum()), max_rel=float(np.max(err / ref)))
+    rel_err = np.where(ref > 0, err / np.where(ref > 0, ref, 1.0), np.where(err > 0, np.inf, 0.0))
+    return (not bad.any()), dict(n=err.size, bad=int(bad.sum()), max_rel=float(np.max(rel_err)))

@@ -15,7 +15,8 @@ from __future__ import annotations
 from . import abi
 from .abi import (  # noqa: F401
     MHCPB_ACCUMULATE_DW, MHCPB_ALLOW_TF32, MHCPB_COMPENSATED_DW, MHCPB_FMA_KERNEL,
-    MHCPB_HAS_ADDEND, MhcpbError, mhcpb_destroy, mhcpb_execute_dx, mhcpb_reduce_dw,
+    MHCPB_HAS_ADDEND, MhcpbError, mhcpb_destroy, mhcpb_execute_dx, mhcpb_forward,
+    mhcpb_forward_workspace_bytes, mhcpb_reduce_dw,
     mhcpb_execute, mhcpb_get_device_status, mhcpb_last_cuda_error, mhcpb_plan_create,
     mhcpb_plan_query, mhcpb_plan_set_max_ctas, mhcpb_plan_set_wait_limit, mhcpb_status_string,
     mhcpb_workspace_bytes,
@@ -84,6 +85,17 @@ class Plan:
         """Second half: dW from the partials in ``workspace``."""
         mhcpb_reduce_dw(self.handle, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                         dw.data_ptr(), self._stream(stream, dw))
+
+    @property
+    def forward_workspace_bytes(self) -> int:
+        return mhcpb_forward_workspace_bytes(self.handle)
+
+    def forward(self, x, w, proj, r, workspace, eps: float = 1e-6, stream=None):
+        """The stage's forward: proj [T, 32] = X W^T (columns 24..31 zero) and
+        r [T] = sqrt(mean X^2 + eps) (see ``mhcpb_forward``)."""
+        mhcpb_forward(self.handle, x.data_ptr(), w.data_ptr(), eps, proj.data_ptr(), r.data_ptr(),
+                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                      self._stream(stream, x))
 
     def device_status(self, clear: bool = False) -> int:
         return mhcpb_get_device_status(self.handle, clear)

@@ -48,7 +48,7 @@ EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcp
             "mhcpb_get_device_status", "mhcpb_plan_query", "mhcpb_plan_set_wait_limit",
             "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error",
             "mhcpb_execute_static_scratch", "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx",
-            "mhcpb_reduce_dw")
+            "mhcpb_reduce_dw", "mhcpb_forward_workspace_bytes", "mhcpb_forward")
 
 
 class MhcpbError(RuntimeError):
@@ -85,6 +85,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_execute_static_scratch.argtypes = [I64, I64, U32, P, P, P, P, P, P, P, P, P]
     lib.mhcpb_execute_dx.argtypes = [P, P, P, P, P, P, P, P, SZ, P, P]
     lib.mhcpb_reduce_dw.argtypes = [P, P, SZ, P, P]
+    lib.mhcpb_forward_workspace_bytes.argtypes = [P, ctypes.POINTER(SZ)]
+    lib.mhcpb_forward.argtypes = [P, P, P, ctypes.c_float, P, P, P, SZ, P]
     lib.mhcpb_destroy.argtypes = [P]
     lib.mhcpb_status_string.argtypes = [I32]
     lib.mhcpb_status_string.restype = ctypes.c_char_p
@@ -93,7 +95,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute",
                  "mhcpb_execute_profiled", "mhcpb_get_device_status", "mhcpb_plan_query",
                  "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch",
-                 "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx", "mhcpb_reduce_dw"):
+                 "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx", "mhcpb_reduce_dw",
+                 "mhcpb_forward_workspace_bytes", "mhcpb_forward"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -142,6 +145,18 @@ def mhcpb_reduce_dw(plan: int, workspace: int, workspace_bytes: int, dw: int,
                     stream: int | None) -> None:
     _check(load().mhcpb_reduce_dw(plan, workspace, int(workspace_bytes), dw, stream or None),
            "mhcpb_reduce_dw")
+
+
+def mhcpb_forward_workspace_bytes(plan: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().mhcpb_forward_workspace_bytes(plan, ctypes.byref(n)), "mhcpb_forward_workspace_bytes")
+    return n.value
+
+
+def mhcpb_forward(plan: int, x: int, w: int, eps: float, proj: int, r: int, workspace: int,
+                  workspace_bytes: int, stream: int | None) -> None:
+    _check(load().mhcpb_forward(plan, x, w, float(eps), proj, r, workspace, int(workspace_bytes),
+                                stream or None), "mhcpb_forward")
 
 
 def mhcpb_get_device_status(plan: int, clear: bool = False) -> int:

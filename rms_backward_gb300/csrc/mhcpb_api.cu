@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -34,6 +35,8 @@ struct mhcpb_plan_s {
     int max_grid = 0;     // default grid of the tensor-core kernel (before any cap)
     uint64_t* d_trace = nullptr;  // timeline stamps (builds with MHCPB_TRACE only)
     size_t trace_bytes = 0;
+    int fwd_grid = 0;     // CTAs of the forward's tensor-core kernel
+    int fwd_max_grid = 0; // its default (before any cap)
 };
 
 namespace {
@@ -241,6 +244,11 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
         }
         p->smem = tc::smem_bytes(add, p->epi_warps);
     }
+    p->fwd_grid = p->fwd_max_grid = fwd::grid_size(T, K, sms);
+    if ((e = fwd::setup()) != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "setup (forward kernel)");
+    }
     if ((e = cudaMalloc(&p->d_status, sizeof(uint32_t))) != cudaSuccess) {
         delete p;
         return cuda_fail(e, "cudaMalloc (status word)");
@@ -431,6 +439,61 @@ mhcpb_status_t mhcpb_reduce_dw(mhcpb_plan_t plan, void* workspace, size_t worksp
                         workspace, workspace_bytes, nullptr, stream, nullptr, nullptr, nullptr);
 }
 
+mhcpb_status_t mhcpb_forward_workspace_bytes(mhcpb_plan_t plan, size_t* bytes) {
+    if (plan == nullptr || bytes == nullptr) return MHCPB_ERR_INVALID_ARG;
+    *bytes = fwd::workspace_bytes(plan->T, plan->K);
+    return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_forward(mhcpb_plan_t plan, const void* x, const float* w, float eps,
+                             float* proj, float* r, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    if (plan == nullptr || !x || !w || !proj || !r || !workspace) return MHCPB_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !(eps < INFINITY)) return MHCPB_ERR_INVALID_ARG;
+    const int64_t T = plan->T, K = plan->K;
+    const size_t ws = fwd::workspace_bytes(T, K);
+    if (workspace_bytes < ws) return MHCPB_ERR_WORKSPACE_TOO_SMALL;
+    const void* ptrs[5] = {x, w, proj, r, workspace};
+    const size_t sizes[5] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4),
+                             (size_t)(T * fwd::kProjCols * 4), (size_t)(T * 4), ws};
+    for (int i = 0; i < 5; ++i)
+        if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != 0) return MHCPB_ERR_MISALIGNED;
+    Range rg[5];
+    for (int i = 0; i < 5; ++i) {
+        rg[i].lo = reinterpret_cast<uintptr_t>(ptrs[i]);
+        rg[i].hi = rg[i].lo + sizes[i];
+    }
+    for (int i = 0; i < 5; ++i)
+        for (int j = i + 1; j < 5; ++j)
+            if (overlap(rg[i], rg[j])) return MHCPB_ERR_ALIASING;
+    for (int i = 0; i < 5; ++i) {
+        mhcpb_status_t s = check_device_ptr(ptrs[i], plan->device);
+        if (s != MHCPB_OK) return s;
+    }
+    if (!get_encode()) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
+    DeviceGuard g(plan->device);
+    if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
+    CUtensorMap xm;
+    if (!encode_bf16_map(&xm, x, T, K, fwd::kTokenTile))
+        return cuda_fail(cudaErrorInvalidValue, "tensor map of x");
+    fwd::FwdParams p{};
+    p.T = (int32_t)T;
+    p.K = (int32_t)K;
+    p.n_tt = (int32_t)((T + fwd::kTokenTile - 1) / fwd::kTokenTile);
+    p.n_fc = (int32_t)fwd::n_chunks(K);
+    p.t_pad = (int32_t)fwd::t_pad(T);
+    p.w = w;
+    p.partial = static_cast<float*>(workspace);
+    p.proj = proj;
+    p.r = r;
+    p.eps = eps;
+    p.status = plan->d_status;
+    p.timeout_ns = plan->timeout_ns;
+    cudaError_t e = fwd::launch(p, xm, plan->fwd_grid, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "launch (forward kernels)");
+    return MHCPB_OK;
+}
+
 mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status, int clear) {
     if (plan == nullptr || status == nullptr) return MHCPB_ERR_INVALID_ARG;
     DeviceGuard g(plan->device);
@@ -450,6 +513,7 @@ mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status
 
 mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas) {
     if (plan == nullptr || max_ctas < 0) return MHCPB_ERR_INVALID_ARG;
+    plan->fwd_grid = (max_ctas == 0 || max_ctas > plan->fwd_max_grid) ? plan->fwd_max_grid : max_ctas;
     if (plan->flags & MHCPB_FMA_KERNEL) return MHCPB_OK;
     plan->grid = (max_ctas == 0 || max_ctas > plan->max_grid) ? plan->max_grid : max_ctas;
     return MHCPB_OK;

@@ -81,6 +81,43 @@ cudaError_t setup();
 cudaError_t launch(const MainParams& p, cudaStream_t stream);
 }  // namespace fma
 
+// Forward of the stage (proj = X W^T over TF32 W, r = RMS of each row):
+// tensor-core kernel plus a fixed-order reduction of per-chunk partials.
+namespace fwd {
+constexpr int kTokenTile = 128;   // MMA M
+constexpr int kChunk = 512;       // columns per work unit (fixed: partials depend only on K)
+constexpr int kBox = 64;          // TMA box width
+constexpr int kPartRows = 25;     // per chunk and token: 24 projections + the sum of squares
+constexpr int kProjCols = 32;     // stored width of proj (columns 24..31 written as zero)
+struct FwdParams {
+    int32_t T;
+    int32_t K;
+    int32_t n_tt;         // token tiles, ceil(T / 128)
+    int32_t n_fc;         // column chunks, ceil(K / 512)
+    int32_t t_pad;        // token stride of the partial rows, T rounded up to 32
+    const float* w;       // [24, K]
+    float* partial;       // [n_fc][25][t_pad]
+    float* proj;          // [T, 32]
+    float* r;             // [T]
+    float eps;
+    uint32_t* status;
+    uint64_t timeout_ns;
+};
+inline int64_t t_pad(int64_t T) { return (T + 31) / 32 * 32; }
+inline int64_t n_chunks(int64_t K) { return (K + kChunk - 1) / kChunk; }
+inline size_t workspace_bytes(int64_t T, int64_t K) {
+    return (size_t)n_chunks(K) * kPartRows * (size_t)t_pad(T) * sizeof(float);
+}
+inline int grid_size(int64_t T, int64_t K, int sms) {
+    const int64_t units = n_chunks(K) * ((T + kTokenTile - 1) / kTokenTile);
+    return (int)(units < sms ? units : sms);
+}
+size_t smem_bytes();
+cudaError_t setup();
+// launches both kernels on `stream`; x_map: X [T, K] BF16, boxes 64 x 128, 128-byte swizzle
+cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, int grid, cudaStream_t stream);
+}  // namespace fwd
+
 // Host helpers shared by the entry points (defined in mhcpb_api.cu).
 // encode_tc_maps: the six tensor maps of the tensor-core kernel; returns the
 // name of the map that failed, or null.  record_cuda_error: stores the

@@ -34,11 +34,12 @@
 //  * Warp roles: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-3 operand
 //    preparation (TF32 rounding and BF16 hi/lo split of P and W into the
 //    tensor-core operand layout, from shared memory), 4.. epilogue.
-//  * Every mbarrier wait is bounded (see wait_bar): on timeout the kernel
+//  * Every mbarrier wait is bounded (wait_bar, mhcpb_wait.cuh): on timeout the kernel
 //    records a status word, drains its own copies and MMAs and exits.
 #include <cuda_bf16.h>
 
 #include "mhcpb_internal.h"
+#include "mhcpb_wait.cuh"
 #include "ptx.cuh"
 
 namespace mhcpb {
@@ -90,28 +91,6 @@ struct Cfg {
     static_assert(stage_bytes % 1024 == 0, "stages must stay 1 KiB aligned");
     static_assert(alloc <= 232448, "shared memory budget");
 };
-
-// Bounded mbarrier wait.  Returns false when the CTA is aborting (another role
-// timed out) or when this wait exceeded the time limit; in the latter case it
-// raises the CTA's abort flag and records the timeout in the status word.
-// With honor_abort == false it keeps waiting (still bounded) while aborting:
-// used to drain a role's own in-flight copies and MMAs before exit.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                      uint32_t* status, uint64_t timeout_ns, bool honor_abort) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((i & 31u) == 0) {
-            if (honor_abort && *abort_flag) return false;
-            if (ptx::globaltimer() - t0 > timeout_ns) {
-                *abort_flag = 1u;
-                atomicCAS(status, kDevOk, kDevTimeout);
-                return false;
-            }
-        }
-    }
-}
 
 // Timeline stamps for instrumented builds (MHCPB_TRACE); nothing otherwise.
 #ifdef MHCPB_TRACE
