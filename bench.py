@@ -50,6 +50,8 @@ def _args():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["training_profile", "long_sublayer", "edge", "fused_addend"],
                     help="the headline is the training profile; the others are extra lines")
+    ap.add_argument("--stage", choices=["backward", "forward"], default="backward",
+                    help="backward (the headline) or the stage's forward (proj and r)")
     ap.add_argument("--compensated-dw", action="store_true",
                     help="plan flag MHCPB_COMPENSATED_DW (TwoSum dW reduction, one rounding)")
     ap.add_argument("--e2e-steps", type=int, default=30)
@@ -439,10 +441,170 @@ def run_ours(args):
     return 0
 
 
+def run_forward(args):
+    """The stage's forward (mhcpb_forward): proj = X W^T and r = RMS(X) on the
+    workload's X and W, same timing rules as the backward."""
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = _dist_env()
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from rms_backward_gb300 import Plan, abi
+
+    cfg = dict(WL.CONFIGS[args.workload])
+    cfg.pop("addend", None)
+    T, K = cfg["T"], cfg["K"]
+    cfg["seed"] += 97 * rank
+    wl = WL.make(args.workload, **cfg)
+    plan = Plan(T, K, local)
+    pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
+    h_x = pin(wl.x.view(np.int16)).view(torch.bfloat16)
+    h_w = pin(wl.w)
+    x, w = h_x.to(dev), h_w.to(dev)
+    proj = torch.empty((T, 32), dtype=torch.float32, device=dev)
+    r = torch.empty((T,), dtype=torch.float32, device=dev)
+    wsb = plan.forward_workspace_bytes
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    eps = 1e-6
+
+    def step():
+        abi.mhcpb_forward(plan.handle, x.data_ptr(), w.data_ptr(), eps, proj.data_ptr(),
+                          r.data_ptr(), ws.data_ptr(), wsb, sh)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if plan.device_status() != 0:
+        raise RuntimeError("device-side timeout during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i & 7))
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    mean_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    if plan.device_status() != 0:
+        raise RuntimeError("device-side timeout during the timed steps")
+    if world > 1:
+        t = torch.tensor([mean_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    alg = WL.algorithmic_bytes_forward(T, K)
+    value = world * alg / (mean_ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+
+    lib = abi.load()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    k1, k2 = [], []
+    for i in range(min(200, args.steps)):
+        flush.fill_(1.0)
+        e0.record(stream)
+        e1.record(stream)
+        e2.record(stream)
+        st = lib.mhcpb_forward_profiled(plan.handle, x.data_ptr(), w.data_ptr(), eps,
+                                        proj.data_ptr(), r.data_ptr(), ws.data_ptr(), wsb, sh,
+                                        e0.cuda_event, e1.cuda_event, e2.cuda_event)
+        if st != 0:
+            raise RuntimeError(f"mhcpb_forward_profiled: {abi.status_string(st)}")
+        e2.synchronize()
+        k1.append(e0.elapsed_time(e1))
+        k2.append(e1.elapsed_time(e2))
+    k1_ms, k2_ms = float(np.mean(k1)), float(np.mean(k2))
+    k1_bytes = 2 * T * K + 96 * K    # kernel 1 reads X and W; kernel 2 writes proj and r
+    k1_gbs = k1_bytes / (k1_ms * 1e-3) / 1e9
+
+    h_proj = torch.empty((T, 32), dtype=torch.float32).pin_memory()
+    h_r = torch.empty((T,), dtype=torch.float32).pin_memory()
+    h2d, d2h = x.numel() * 2 + w.numel() * 4, proj.numel() * 4 + r.numel() * 4
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(args.e2e_steps):
+        x.copy_(h_x, non_blocking=True)
+        w.copy_(h_w, non_blocking=True)
+        step()
+        h_proj.copy_(proj, non_blocking=True)
+        h_r.copy_(r, non_blocking=True)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+    e2e_value = world * alg / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle.mhcpf_oracle as F
+        done, secs, nbytes, i = 0, 0.0, 0, 0
+        while secs < 10.0 and done < T:
+            piece = WL.make("cpu_sample", T=256, K=K, seed=cfg["seed"] + 1000 * i)
+            t0 = time.perf_counter()
+            F.mhc_proj_forward(piece.x, piece.w)
+            secs += time.perf_counter() - t0
+            done += 256
+            nbytes += WL.algorithmic_bytes_forward(256, K)
+            i += 1
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": _cpu_threads(), "kind": "oracle",
+               "sample": f"{done} of {T} tokens x K={K} (256-token slices, {secs:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": f"mHC proj-fwd achieved HBM GB/s at T={T}, K={K} ({args.workload})",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": mean_ms, "us_per_step": mean_ms * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"forward, {args.workload} T={T} K={K} (4 streams x hidden 5120)",
+                       "T": T, "K": K, "eps": eps,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                       "algorithmic_bytes_per_step": alg,
+                       "pct_of_hbm_peak": 100.0 * (value / world) / peak,
+                       "wall_s_timed_region": wall},
+            "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": k1_gbs / peak, "traffic": None,
+                         "kernel": "forward streaming kernel (projection + squares, partials)",
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel_us": k1_ms * 1e3, "reduce_us": k2_ms * 1e3,
+                         "algorithmic_bytes_per_launch": k1_bytes},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    plan.close()
+    return 0
+
+
 def main():
     args = _args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.stage == "forward":
+        return run_forward(args)
     return run_ours(args)
 
 

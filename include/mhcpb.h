@@ -286,6 +286,13 @@ mhcpb_status_t mhcpb_forward_workspace_bytes(mhcpb_plan_t plan, size_t* bytes);
 mhcpb_status_t mhcpb_forward(mhcpb_plan_t plan, const void* x, const float* w, float eps,
                              float* proj, float* r, void* workspace, size_t workspace_bytes,
                              void* stream);
+/* mhcpb_forward with timing events for measurement tools (cudaEvent_t, each
+ * may be NULL): recorded before the streaming kernel, between the two
+ * kernels and after the reduction, on `stream`. */
+mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const float* w, float eps,
+                                      float* proj, float* r, void* workspace,
+                                      size_t workspace_bytes, void* stream, void* ev_before,
+                                      void* ev_between, void* ev_after);
 
 /* Releases the plan (and its status word).  Safe on NULL. */
 mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan);

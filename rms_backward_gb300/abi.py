@@ -48,7 +48,8 @@ EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcp
             "mhcpb_get_device_status", "mhcpb_plan_query", "mhcpb_plan_set_wait_limit",
             "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error",
             "mhcpb_execute_static_scratch", "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx",
-            "mhcpb_reduce_dw", "mhcpb_forward_workspace_bytes", "mhcpb_forward")
+            "mhcpb_reduce_dw", "mhcpb_forward_workspace_bytes", "mhcpb_forward",
+            "mhcpb_forward_profiled")
 
 
 class MhcpbError(RuntimeError):
@@ -87,6 +88,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_reduce_dw.argtypes = [P, P, SZ, P, P]
     lib.mhcpb_forward_workspace_bytes.argtypes = [P, ctypes.POINTER(SZ)]
     lib.mhcpb_forward.argtypes = [P, P, P, ctypes.c_float, P, P, P, SZ, P]
+    lib.mhcpb_forward_profiled.argtypes = [P, P, P, ctypes.c_float, P, P, P, SZ, P, P, P, P]
     lib.mhcpb_destroy.argtypes = [P]
     lib.mhcpb_status_string.argtypes = [I32]
     lib.mhcpb_status_string.restype = ctypes.c_char_p
@@ -96,7 +98,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "mhcpb_execute_profiled", "mhcpb_get_device_status", "mhcpb_plan_query",
                  "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch",
                  "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx", "mhcpb_reduce_dw",
-                 "mhcpb_forward_workspace_bytes", "mhcpb_forward"):
+                 "mhcpb_forward_workspace_bytes", "mhcpb_forward", "mhcpb_forward_profiled"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib

@@ -445,9 +445,9 @@ mhcpb_status_t mhcpb_forward_workspace_bytes(mhcpb_plan_t plan, size_t* bytes) {
     return MHCPB_OK;
 }
 
-mhcpb_status_t mhcpb_forward(mhcpb_plan_t plan, const void* x, const float* w, float eps,
-                             float* proj, float* r, void* workspace, size_t workspace_bytes,
-                             void* stream) {
+static mhcpb_status_t forward_impl(mhcpb_plan_t plan, const void* x, const float* w, float eps,
+                                   float* proj, float* r, void* workspace, size_t workspace_bytes,
+                                   void* stream, void* ev0, void* ev1, void* ev2) {
     if (plan == nullptr || !x || !w || !proj || !r || !workspace) return MHCPB_ERR_INVALID_ARG;
     if (!(eps >= 0.f) || !(eps < INFINITY)) return MHCPB_ERR_INVALID_ARG;
     const int64_t T = plan->T, K = plan->K;
@@ -473,9 +473,11 @@ mhcpb_status_t mhcpb_forward(mhcpb_plan_t plan, const void* x, const float* w, f
     if (!get_encode()) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
     DeviceGuard g(plan->device);
     if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
-    CUtensorMap xm;
+    CUtensorMap xm, wm;
     if (!encode_bf16_map(&xm, x, T, K, fwd::kTokenTile))
         return cuda_fail(cudaErrorInvalidValue, "tensor map of x");
+    if (!encode_f32_map(&wm, w, kNProj, (int)K, fwd::kBox, kNProj))
+        return cuda_fail(cudaErrorInvalidValue, "tensor map of w");
     fwd::FwdParams p{};
     p.T = (int32_t)T;
     p.K = (int32_t)K;
@@ -489,9 +491,27 @@ mhcpb_status_t mhcpb_forward(mhcpb_plan_t plan, const void* x, const float* w, f
     p.eps = eps;
     p.status = plan->d_status;
     p.timeout_ns = plan->timeout_ns;
-    cudaError_t e = fwd::launch(p, xm, plan->fwd_grid, reinterpret_cast<cudaStream_t>(stream));
+    p.trace = plan->d_trace;
+    cudaError_t e = fwd::launch(p, xm, wm, plan->fwd_grid, reinterpret_cast<cudaStream_t>(stream),
+                                reinterpret_cast<cudaEvent_t>(ev0), reinterpret_cast<cudaEvent_t>(ev1),
+                                reinterpret_cast<cudaEvent_t>(ev2));
     if (e != cudaSuccess) return cuda_fail(e, "launch (forward kernels)");
     return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_forward(mhcpb_plan_t plan, const void* x, const float* w, float eps,
+                             float* proj, float* r, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    return forward_impl(plan, x, w, eps, proj, r, workspace, workspace_bytes, stream, nullptr,
+                        nullptr, nullptr);
+}
+
+mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const float* w, float eps,
+                                      float* proj, float* r, void* workspace,
+                                      size_t workspace_bytes, void* stream, void* ev_before,
+                                      void* ev_between, void* ev_after) {
+    return forward_impl(plan, x, w, eps, proj, r, workspace, workspace_bytes, stream, ev_before,
+                        ev_between, ev_after);
 }
 
 mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status, int clear) {

@@ -102,6 +102,7 @@ struct FwdParams {
     float eps;
     uint32_t* status;
     uint64_t timeout_ns;
+    uint64_t* trace;      // timeline stamps, only in builds with MHCPB_TRACE (else null)
 };
 inline int64_t t_pad(int64_t T) { return (T + 31) / 32 * 32; }
 inline int64_t n_chunks(int64_t K) { return (K + kChunk - 1) / kChunk; }
@@ -114,8 +115,11 @@ inline int grid_size(int64_t T, int64_t K, int sms) {
 }
 size_t smem_bytes();
 cudaError_t setup();
-// launches both kernels on `stream`; x_map: X [T, K] BF16, boxes 64 x 128, 128-byte swizzle
-cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, int grid, cudaStream_t stream);
+// launches both kernels on `stream`; x_map: X [T, K] BF16, boxes 64 x 128, 128-byte swizzle;
+// w_map: W [24, K] FP32, boxes 64 x 24, no swizzle; non-null events are
+// recorded before, between and after the two kernels
+cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorMap& w_map, int grid,
+                   cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, cudaEvent_t ev2);
 }  // namespace fwd
 
 // Host helpers shared by the entry points (defined in mhcpb_api.cu).

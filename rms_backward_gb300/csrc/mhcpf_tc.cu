@@ -22,8 +22,9 @@
 //    the TF32 product), is the K-major B operand [Wh; Wl] (N = 48).  The
 //    unit's 8 boxes accumulate into one TMEM accumulator (double-buffered
 //    across units); proj = D[:, j] + D[:, 24 + j];
-//  * warps 2-3: W preparation (TF32 rounding, hi/lo split, 128-byte-swizzled
-//    K-major layout);
+//  * warps 2-3: W preparation: each chunk of W is fetched by TMA (FP32, one
+//    chunk ahead) and converted in shared memory (TF32 rounding, hi/lo split,
+//    128-byte-swizzled K-major layout);
 //  * warps 4-7: per token row, the sum of squares of the X box from shared
 //    memory (eight 8-term partial sums, then their sum: a shallow FP32 sum),
 //    and at the end of each unit the drain of the accumulator; they write
@@ -31,7 +32,8 @@
 //    to the workspace.
 // Kernel 2 sums each token's partials over the chunks in ascending order and
 // writes proj and r (programmatic dependent launch, like the backward's
-// reduction).  Every mbarrier wait is bounded (wait_bar).
+// reduction), then drops the dead partial lines from L2.  Every mbarrier wait
+// is bounded (wait_bar).
 #include <cuda_bf16.h>
 
 #include "mhcpb_internal.h"
@@ -46,17 +48,39 @@ namespace {
 constexpr int kBoxes = kChunk / kBox;                 // 8 boxes per unit
 constexpr uint32_t kBoxBytes = kTokenTile * kBox * 2;  // 16 KiB
 constexpr uint32_t kWBoxBytes = 48 * kBox * 2;         // 6 KiB: [Wh; Wl] rows x 64 columns
-constexpr int kNS = 10;                                // X pipeline stages (one box each)
+constexpr int kNS = 7;                                 // X pipeline stages (one box each)
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 128;                    // two accumulators of 64 columns
+constexpr uint32_t kWRawBox = kNProj * kBox * 4;       // 6 KiB: FP32 W rows x 64 columns
 constexpr uint32_t kOffW = kNS * kBoxBytes;
-constexpr uint32_t kOffBar = kOffW + kBoxes * kWBoxBytes;
-// barriers: x_full[NS] x_empty[NS] acc_full[2] acc_empty[2] w_full w_empty fin
+constexpr uint32_t kOffWRaw = kOffW + kBoxes * kWBoxBytes;
+constexpr uint32_t kOffBar = kOffWRaw + kBoxes * kWRawBox;
+// barriers: x_full[NS] x_empty[NS] acc_full[2] acc_empty[2] w_full w_empty fin w_raw
+// (w_raw: a chunk of W as stored, FP32, landed by TMA; it is fetched one chunk
+// ahead, while the MMAs still use the previous chunk's converted W)
 constexpr int B_XF = 0, B_XE = kNS, B_AF = 2 * kNS, B_AE = 2 * kNS + 2, B_WF = 2 * kNS + 4,
-              B_WE = 2 * kNS + 5, B_FIN = 2 * kNS + 6, kBars = 2 * kNS + 7;
+              B_WE = 2 * kNS + 5, B_FIN = 2 * kNS + 6, B_WR = 2 * kNS + 7, kBars = 2 * kNS + 8;
 constexpr uint32_t kOffMisc = kOffBar + kBars * 8;
 constexpr uint32_t kSmem = kOffMisc + 16 + 1024;        // + room to align the base to 1 KiB
 static_assert(kSmem <= 232448, "shared memory budget");
+
+// Timeline stamps for instrumented builds (MHCPB_TRACE); nothing otherwise.
+#ifdef MHCPB_TRACE
+#define FTRACE(ev, n)                                                                       \
+    do {                                                                                    \
+        if (p.trace != nullptr && (n) < kTraceTiles)                                       \
+            p.trace[((size_t)blockIdx.x * kTraceEvents + (ev)) * kTraceTiles + (n)] =      \
+                ptx::globaltimer();                                                         \
+    } while (0)
+#else
+#define FTRACE(ev, n) \
+    do {              \
+    } while (0)
+#endif
+enum FwdTraceEvent {
+    F_PROD_ISSUE = 0, F_MMA_XFULL, F_MMA_COMMIT, F_SS_XFULL, F_SS_DONE, F_PROD_XEMPTY,
+    F_W_READY, F_DRAIN_START, F_DRAIN_END, F_CTA_START, F_CTA_END   // boxes; W by chunk; drains by unit
+};
 
 struct Unit {
     int fc, tt, nb;   // chunk, token tile, boxes inside K
@@ -77,7 +101,8 @@ __device__ __forceinline__ float tf32_rna(float v) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap xmap) {
+    fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap xmap,
+                  const __grid_constant__ CUtensorMap wmap) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -92,8 +117,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u_begin = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
     const int u_end = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
     const uint64_t tmo = p.timeout_ns;
+    // one chunk of W as stored (eight 64-column FP32 boxes, zero past K) into
+    // the raw buffer, L2 evict-last: every token tile re-reads W
+    auto fetch_raw_w = [&](int fc) {
+        const uint64_t pol_keep = ptx::policy_evict_last();
+        ptx::mbar_arrive_expect_tx(bar(B_WR), kBoxes * kWRawBox);
+        for (int b = 0; b < kBoxes; ++b)
+            ptx::tma_load_2d(sbase + kOffWRaw + (uint32_t)b * kWRawBox, &wmap, fc * kChunk + b * kBox,
+                             0, bar(B_WR), pol_keep);
+    };
 
     if (threadIdx.x == 0) {
+        FTRACE(F_CTA_START, 0);
         for (int s = 0; s < kNS; ++s) {
             ptx::mbar_init(bar(B_XF + s), 1);
             ptx::mbar_init(bar(B_XE + s), 1 + 4);   // the MMAs' commit + 4 sum-of-squares warps
@@ -105,9 +140,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(B_WF), 2);
         ptx::mbar_init(bar(B_WE), 1);
         ptx::mbar_init(bar(B_FIN), 1);
+        ptx::mbar_init(bar(B_WR), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&xmap);
+        ptx::prefetch_tensormap(&wmap);
+        // the first chunk of W goes out before any X load: the MMAs cannot start
+        // (nor release a stage) before it is converted
+        if (u_begin < u_end) fetch_raw_w(unit_at(p, u_begin).fc);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
@@ -134,9 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    FTRACE(F_PROD_XEMPTY, n);
                     ptx::mbar_arrive_expect_tx(bar(B_XF + st), kBoxBytes);
                     ptx::tma_load_2d(sbase + (uint32_t)st * kBoxBytes, &xmap,
                                      U.fc * kChunk + b * kBox, U.tt * kTokenTile, bar(B_XF + st), pol);
+                    FTRACE(F_PROD_ISSUE, n);
                     issued |= 1u << st;
                     last_par = (last_par & ~(1u << st)) | (ph << st);
                     if (++st == kNS) { st = 0; ph ^= 1u; }
@@ -152,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 48, false, false);
             const uint32_t w_base = sbase + kOffW;
-            int st = 0, ab = 0, n_w = 0, prev_fc = -1;
+            int st = 0, ab = 0, n_w = 0, prev_fc = -1, n = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
             for (int u = u_begin; u < u_end && ok; ++u) {
@@ -170,11 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t d = tmem + (uint32_t)ab * 64u;
-                for (int b = 0; b < U.nb; ++b) {
+                for (int b = 0; b < U.nb; ++b, ++n) {
                     if (!wait_bar(bar(B_XF + st), ph, abort_flag, p.status, tmo, true)) {
                         ok = false;
                         break;
                     }
+                    FTRACE(F_MMA_XFULL, n);
                     ptx::tc_fence_after();
                     const uint32_t xa = sbase + (uint32_t)st * kBoxBytes;
                     const uint32_t wb = w_base + (uint32_t)b * kWBoxBytes;
@@ -186,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_bf16(d, da, db, idesc, (b > 0 || k > 0) ? 1u : 0u);
                     }
                     ptx::tc_commit(bar(B_XE + st));
+                    FTRACE(F_MMA_COMMIT, n);
                     if (++st == kNS) { st = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
@@ -200,41 +244,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------- W preparation
-        // thread = one of the chunk box's 64 columns; rows j (hi) and 24 + j (lo)
-        const int col = (warp - 2) * 32 + lane;
-        int n_w = 0, prev_fc = -1;
+        // Each chunk of W arrives raw (FP32) by TMA, one chunk ahead: thread 0
+        // fetched the first one before the block-wide sync, lane 0 of warp 2
+        // fetches each later one once the raw buffer has been converted.  Both
+        // warps convert (four columns of one W row per step) into the swizzled
+        // operand buffer, once the MMAs of the previous chunk are done with it.
+        const int tid = (warp - 2) * 32 + lane;   // 0..63
+        const bool fetcher = warp == 2 && lane == 0;
+        int n_w = 0, prev_fc = -1, n_raw = u_begin < u_end ? 1 : 0;
         bool ok = true;
         for (int u = u_begin; u < u_end && ok; ++u) {
             const Unit U = unit_at(p, u);
             if (U.fc == prev_fc) continue;
             prev_fc = U.fc;
-            if (n_w > 0 &&
-                !wait_bar(bar(B_WE), (uint32_t)(n_w - 1) & 1u, abort_flag, p.status, tmo, true)) {
+            if (!wait_bar(bar(B_WR), (uint32_t)n_w & 1u, abort_flag, p.status, tmo, true) ||
+                (n_w > 0 &&
+                 !wait_bar(bar(B_WE), (uint32_t)(n_w - 1) & 1u, abort_flag, p.status, tmo, true))) {
                 ok = false;
                 break;
             }
+            const float4* raw = reinterpret_cast<const float4*>(smem + kOffWRaw);
             uint8_t* wsm = smem + kOffW;
-            for (int b = 0; b < kBoxes; ++b) {
-                const int k = U.fc * kChunk + b * kBox + col;
-                uint8_t* box = wsm + b * kWBoxBytes;
-                // 128-byte swizzle: 16-byte chunk c of row n sits at chunk c ^ (n & 7)
-                const int c16 = col >> 3, within = (col & 7) * 2;
-#pragma unroll 4
-                for (int j = 0; j < kNProj; ++j) {
-                    const float v = k < p.K ? tf32_rna(__ldg(p.w + (size_t)j * p.K + k)) : 0.f;
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-                    const float rem = isfinite(v) ? v - __bfloat162float(hi) : 0.f;
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(rem);
-                    const int nh = j, nl = kNProj + j;
-                    *reinterpret_cast<__nv_bfloat16*>(box + nh * 128 + ((c16 ^ (nh & 7)) << 4) + within) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(box + nl * 128 + ((c16 ^ (nl & 7)) << 4) + within) = lo;
+            // per box: 24 rows x 16 float4 = 384 float4, six per thread
+#pragma unroll 2
+            for (int i = tid; i < kBoxes * kNProj * (kBox / 4); i += 64) {
+                const int b = i / (kNProj * (kBox / 4));
+                const int rem = i - b * (kNProj * (kBox / 4));
+                const int j = rem >> 4, c4 = rem & 15;   // row, group of 4 columns
+                const float4 v4 = raw[i];
+                const float v[4] = {tf32_rna(v4.x), tf32_rna(v4.y), tf32_rna(v4.z), tf32_rna(v4.w)};
+                uint32_t hi[2], lo[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                    hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+                    const float r0 = isfinite(v[2 * e]) ? v[2 * e] - __low2float(h) : 0.f;
+                    const float r1 = isfinite(v[2 * e + 1]) ? v[2 * e + 1] - __high2float(h) : 0.f;
+                    const __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+                    lo[e] = *reinterpret_cast<const uint32_t*>(&l);
                 }
+                // 128-byte swizzle: 16-byte chunk c of row n sits at chunk c ^ (n & 7);
+                // four columns are 8 bytes, half a chunk
+                uint8_t* box = wsm + b * kWBoxBytes;
+                const int c16 = c4 >> 1, half = (c4 & 1) * 8;
+                const int nh = j, nl = kNProj + j;
+                *reinterpret_cast<uint2*>(box + nh * 128 + ((c16 ^ (nh & 7)) << 4) + half) = make_uint2(hi[0], hi[1]);
+                *reinterpret_cast<uint2*>(box + nl * 128 + ((c16 ^ (nl & 7)) << 4) + half) = make_uint2(lo[0], lo[1]);
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_WF));
+            if (fetcher) FTRACE(F_W_READY, n_w);
             ++n_w;
+            // the raw buffer is free once both warps have converted it: fetch the
+            // next chunk this CTA will need
+            int next_fc = -1;
+            for (int v = u + 1; v < u_end; ++v) {
+                const int f = unit_at(p, v).fc;
+                if (f != U.fc) { next_fc = f; break; }
+            }
+            if (fetcher && next_fc >= 0) {
+                if (!wait_bar(bar(B_WF), (uint32_t)(n_w - 1) & 1u, abort_flag, p.status, tmo, true)) {
+                    ok = false;
+                } else {
+                    fetch_raw_w(next_fc);
+                    ++n_raw;
+                }
+            }
+            __syncwarp();
         }
+        // every raw W fetch has landed before the CTA exits
+        if (fetcher && n_raw > n_w)
+            wait_bar(bar(B_WR), (uint32_t)(n_raw - 1) & 1u, abort_flag, p.status, tmo, false);
         __syncwarp();
     } else {
         // ---------------------------------------------------------- sum of squares, drain
@@ -242,17 +323,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = q * 32 + lane;              // row within the token tile
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const uint64_t pol_keep = ptx::policy_evict_last();
-        int st = 0, ab = 0;
+        int st = 0, ab = 0, n = 0, un = 0;
         uint32_t ph = 0, aph = 0;
         bool ok = true;
-        for (int u = u_begin; u < u_end && ok; ++u) {
+        for (int u = u_begin; u < u_end && ok; ++u, ++un) {
             const Unit U = unit_at(p, u);
             float ss = 0.f;
-            for (int b = 0; b < U.nb; ++b) {
+            for (int b = 0; b < U.nb; ++b, ++n) {
                 if (!wait_bar(bar(B_XF + st), ph, abort_flag, p.status, tmo, true)) {
                     ok = false;
                     break;
                 }
+                if (q == 0 && lane == 0) FTRACE(F_SS_XFULL, n);
                 const uint8_t* row = smem + (uint32_t)st * kBoxBytes + rr * 128;
                 float part[8];
 #pragma unroll
@@ -272,9 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ss += ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(B_XE + st));
+                if (q == 0 && lane == 0) FTRACE(F_SS_DONE, n);
                 if (++st == kNS) { st = 0; ph ^= 1u; }
             }
             if (!ok) break;
+            if (q == 0 && lane == 0) FTRACE(F_DRAIN_START, un);
             if (!wait_bar(bar(B_AF + ab), aph, abort_flag, p.status, tmo, true)) {
                 ok = false;
                 break;
@@ -304,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::st_global_hint(dst + (size_t)kNProj * p.t_pad, ss, pol_keep);
             }
+            if (q == 0 && lane == 0) FTRACE(F_DRAIN_END, un);
             if (++ab == 2) { ab = 0; aph ^= 1u; }
         }
         __syncwarp();
@@ -314,62 +399,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
+        if (lane == 0) FTRACE(F_CTA_END, 0);
     }
 }
 
 // proj[t][j] = sum over chunks ascending of partial[fc][j][t]; r from the
-// summed squares.  Thread = (partial row j' in 0..24, four tokens).
+// summed squares.  Thread = (partial row j' in 0..24, token t); a warp reads
+// 128 contiguous bytes of a chunk's row per load.
 constexpr int kReduceThreads = 256;
-constexpr int kGroup = 8;
+constexpr int kGroup = 20;   // chunk partials loaded before they are summed
 
 __global__ void __launch_bounds__(kReduceThreads)
-    fwd_reduce_kernel(const float4* __restrict__ part, float* __restrict__ proj,
-                      float* __restrict__ r, int T, int t4_count, int t_pad, int n_fc, float kf,
-                      float eps, int discard) {
+    fwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ proj,
+                      float* __restrict__ r, int T, int t_pad, int n_fc, float kf, float eps,
+                      int discard) {
     ptx::grid_dependency_wait();
     const int64_t i = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x;
-    const bool valid = i < (int64_t)kPartRows * t4_count;
-    const int row = valid ? (int)(i / t4_count) : 0;   // j' (24 = sum of squares)
-    const int t4 = valid ? (int)(i - (int64_t)row * t4_count) : 0;
-    const int64_t stride4 = (int64_t)kPartRows * (t_pad / 4);   // float4s per chunk
-    const int64_t base4 = (int64_t)row * (t_pad / 4) + t4;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool valid = i < (int64_t)kPartRows * t_pad;   // t_pad % 32 == 0: whole warps
+    const int row = valid ? (int)(i / t_pad) : 0;       // j' (24 = sum of squares)
+    const int t = valid ? (int)(i - (int64_t)row * t_pad) : 0;
+    const int64_t stride = (int64_t)kPartRows * t_pad;   // floats per chunk
+    const int64_t base = (int64_t)row * t_pad + t;
+    float a = 0.f;
     for (int f0 = 0; valid && f0 < n_fc; f0 += kGroup) {
-        float4 b[kGroup];
+        float b[kGroup];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
-            if (f0 + g < n_fc) b[g] = part[(int64_t)(f0 + g) * stride4 + base4];
+            if (f0 + g < n_fc) b[g] = part[(int64_t)(f0 + g) * stride + base];
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-            if (f0 + g < n_fc) {
-                if (f0 + g == 0) {
-                    a = b[g];
-                } else {
-                    a.x += b[g].x; a.y += b[g].y; a.z += b[g].z; a.w += b[g].w;
-                }
-            }
+        for (int g = 0; g < kGroup; ++g)
+            if (f0 + g < n_fc) a = (f0 + g == 0) ? b[g] : a + b[g];
+    }
+    if (valid && t < T) {
+        if (row < kNProj) {
+            proj[(size_t)t * kProjCols + row] = a;
+        } else {
+            r[t] = sqrtf(a / kf + eps);   // the mean of the squares, eps, root
+            float4* pad = reinterpret_cast<float4*>(proj + (size_t)t * kProjCols + kNProj);
+            pad[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            pad[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    if (valid) {
-        const float v[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int t = t4 * 4 + e;
-            if (t >= T) break;
-            if (row < kNProj) {
-                proj[(size_t)t * kProjCols + row] = v[e];
-            } else {
-                r[t] = sqrtf(v[e] / kf + eps);   // the mean of the squares, eps, root
-#pragma unroll
-                for (int c = kNProj; c < kProjCols; ++c) proj[(size_t)t * kProjCols + c] = 0.f;
-            }
-        }
-    }
-    // the partials are dead once read: drop their L2 lines (eight float4 of a
-    // line belong to eight consecutive threads of this warp)
+    // the partials are dead once read: drop their L2 lines (a line is one
+    // chunk's row for the 32 tokens of this warp)
     __syncwarp();
-    if (valid && discard && (t4 & 7) == 0) {
-        for (int f = 0; f < n_fc; ++f) ptx::discard_l2_line(part + (int64_t)f * stride4 + base4);
+    if (valid && discard && (t & 31) == 0) {
+        for (int f = 0; f < n_fc; ++f) ptx::discard_l2_line(part + (int64_t)f * stride + base);
     }
 }
 
@@ -381,12 +456,14 @@ cudaError_t setup() {
     return cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
 }
 
-cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, int grid, cudaStream_t stream) {
-    fwd_tc_kernel<<<grid, kThreads, kSmem, stream>>>(p, x_map);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int t4_count = p.t_pad / 4;
-    const int64_t n = (int64_t)kPartRows * t4_count;
+cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorMap& w_map, int grid,
+                   cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, cudaEvent_t ev2) {
+    cudaError_t e;
+    if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return e;
+    fwd_tc_kernel<<<grid, kThreads, kSmem, stream>>>(p, x_map, w_map);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return e;
+    const int64_t n = (int64_t)kPartRows * p.t_pad;
     // discard needs 128-byte lines: t_pad is a multiple of 32 floats
     const int discard = (reinterpret_cast<uintptr_t>(p.partial) & 127u) == 0 ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
@@ -399,9 +476,12 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, int grid, cudaS
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_reduce_kernel, reinterpret_cast<const float4*>(p.partial),
-                              p.proj, p.r, p.T, t4_count, p.t_pad, p.n_fc, (float)p.K, p.eps,
-                              discard);
+    if ((e = cudaLaunchKernelEx(&cfg, fwd_reduce_kernel, static_cast<const float*>(p.partial),
+                                p.proj, p.r, p.T, p.t_pad, p.n_fc, (float)p.K, p.eps, discard)) !=
+        cudaSuccess)
+        return e;
+    if (ev2 && (e = cudaEventRecord(ev2, stream)) != cudaSuccess) return e;
+    return cudaSuccess;
 }
 
 }  // namespace fwd

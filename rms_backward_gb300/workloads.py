@@ -175,6 +175,12 @@ def algorithmic_bytes(T: int, K: int, addend: bool = False) -> int:
     return b
 
 
+def algorithmic_bytes_forward(T: int, K: int) -> int:
+    """Compulsory HBM bytes of one forward: read X (2TK) and W (96K), write
+    proj [T, 32] FP32 (128T) and r (4T)."""
+    return 2 * T * K + 96 * K + 128 * T + 4 * T
+
+
 def algorithmic_flops(T: int, K: int) -> int:
     """Two rank-24 contractions (2*24 FMAs per X element) plus the RMS term."""
     return 4 * T * N_PROJ * K + 2 * T * K
