@@ -484,6 +484,17 @@ def run_forward(args):
     torch.cuda.synchronize()
     if plan.device_status() != 0:
         raise RuntimeError("device-side timeout during warm-up")
+    if args.quick:
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            step()
+        torch.cuda.synchronize()
+        status = plan.device_status()
+        if rank == 0:
+            print(json.dumps({"quick": True, "stage": "forward", "steps": args.steps,
+                              "status": status}), flush=True)
+        plan.close()
+        return 0 if status == 0 else 1
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.25)
