@@ -68,6 +68,27 @@ def _dist_env():
     return rank, world, local
 
 
+def _max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' values (all ranks get it); x itself at N = 1."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _replica_seed(seed: int, rank: int) -> int:
+    """Every replica draws its own inputs."""
+    return seed + 97 * rank
+
+
+def _aggregate_gbs(bytes_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the bytes all ranks moved over the slowest rank's time."""
+    return world * bytes_per_rank / (max_ms * 1e-3) / 1e9
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -254,7 +275,7 @@ def run_ours(args):
 
     cfg = dict(WL.CONFIGS[args.workload])
     T, K = cfg["T"], cfg["K"]
-    cfg["seed"] += 97 * rank           # every replica draws its own inputs
+    cfg["seed"] = _replica_seed(cfg["seed"], rank)
     wl = WL.make(args.workload, **cfg)
     has_add = wl.has_addend
     plan = Plan(T, K, local, addend=has_add, fma_kernel=(args.kernel == "fma"),
@@ -324,14 +345,10 @@ def run_ours(args):
     step_ms = np.array([a.elapsed_time(b) for a, b in ev])
     if plan.device_status() != 0:
         raise RuntimeError("device-side timeout during the timed steps")
-    mean_ms = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([mean_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = _max_over_ranks(float(step_ms.mean()), world)
 
     alg = WL.algorithmic_bytes(T, K, addend=has_add)
-    value = world * alg / (mean_ms * 1e-3) / 1e9
+    value = _aggregate_gbs(alg, world, mean_ms)
     peak, peak_kind = _peaks()
 
     # dominant kernel (the streaming kernel) timed alone: events around each kernel
@@ -387,12 +404,8 @@ def run_ours(args):
         h_dw.copy_(dw, non_blocking=True)
     eb.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * alg / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = _max_over_ranks(ea.elapsed_time(eb) / args.e2e_steps, world)
+    e2e_value = _aggregate_gbs(alg, world, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
@@ -458,7 +471,7 @@ def run_forward(args):
     cfg = dict(WL.CONFIGS[args.workload])
     cfg.pop("addend", None)
     T, K = cfg["T"], cfg["K"]
-    cfg["seed"] += 97 * rank
+    cfg["seed"] = _replica_seed(cfg["seed"], rank)
     wl = WL.make(args.workload, **cfg)
     plan = Plan(T, K, local)
     pin = lambda a: torch.from_numpy(a).pin_memory()  # noqa: E731
@@ -517,12 +530,9 @@ def run_forward(args):
     mean_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     if plan.device_status() != 0:
         raise RuntimeError("device-side timeout during the timed steps")
-    if world > 1:
-        t = torch.tensor([mean_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = _max_over_ranks(mean_ms, world)
     alg = WL.algorithmic_bytes_forward(T, K)
-    value = world * alg / (mean_ms * 1e-3) / 1e9
+    value = _aggregate_gbs(alg, world, mean_ms)
     peak, peak_kind = _peaks()
 
     lib = abi.load()
@@ -558,8 +568,10 @@ def run_forward(args):
         h_r.copy_(r, non_blocking=True)
     eb.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
-    e2e_value = world * alg / (e2e_ms * 1e-3) / 1e9
+    if world > 1:
+        dist.barrier()
+    e2e_ms = _max_over_ranks(ea.elapsed_time(eb) / args.e2e_steps, world)
+    e2e_value = _aggregate_gbs(alg, world, e2e_ms)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
