@@ -31,7 +31,6 @@ struct mhcpb_plan_s {
     size_t smem = 0;
     uint32_t* d_status = nullptr;
     uint64_t timeout_ns = 1000000000ull;  // 1 s bound on every in-kernel wait
-    int epi_warps = 8;    // epilogue warps of the tensor-core kernel (4 or 8)
     int max_grid = 0;     // default grid of the tensor-core kernel (before any cap)
     uint64_t* d_trace = nullptr;  // timeline stamps (builds with MHCPB_TRACE only)
     size_t trace_bytes = 0;
@@ -237,12 +236,11 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
         p->half_units = tc::use_half_units(items, sms) ? 1 : 0;
         p->grid = tc::grid_size(items, sms);
         p->max_grid = p->grid;
-        if (const char* ev = std::getenv("MHCPB_EPI_WARPS")) p->epi_warps = std::atoi(ev) == 4 ? 4 : 8;
-        if ((e = tc::setup(add, p->epi_warps)) != cudaSuccess) {
+        if ((e = tc::setup(add)) != cudaSuccess) {
             delete p;
             return cuda_fail(e, "setup (tensor-core kernel)");
         }
-        p->smem = tc::smem_bytes(add, p->epi_warps);
+        p->smem = tc::smem_bytes(add);
     }
     p->fwd_grid = p->fwd_max_grid = fwd::grid_size(T, K, sms);
     if ((e = fwd::setup()) != cudaSuccess) {
@@ -391,7 +389,7 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, int what, const void* x, c
             if (const char* bad = encode_maps(m, T, K, x, dx, add ? grad_x_addend : x, grad_proj,
                                               grad_r, r))
                 return cuda_fail(cudaErrorInvalidValue, bad);
-            e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], plan->grid, plan->epi_warps, st);
+            e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], plan->grid, st);
             if (e != cudaSuccess) return cuda_fail(e, "launch (tensor-core kernel)");
         }
     }

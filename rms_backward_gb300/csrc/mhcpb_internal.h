@@ -63,13 +63,13 @@ inline int grid_size(int64_t items, int sms) {
     const int64_t units = use_half_units(items, sms) ? 2 * items : items;
     return (int)(units < sms ? units : sms);
 }
-size_t smem_bytes(bool has_addend, int epi_warps);
-cudaError_t setup(bool has_addend, int epi_warps);
+size_t smem_bytes(bool has_addend);
+cudaError_t setup(bool has_addend);
 // Tensor maps: x/dx/addend BF16 [T,K] boxes 64 x {128,32,128} (128-byte swizzle),
 // grad_proj FP32 [T,32] box 24 x 128, grad_r and r FP32 [T] boxes of 128.
 cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensorMap& dx_map,
                    const CUtensorMap& add_map, const CUtensorMap& gp_map, const CUtensorMap& gr_map,
-                   const CUtensorMap& r_map, int grid, int epi_warps, cudaStream_t stream);
+                   const CUtensorMap& r_map, int grid, cudaStream_t stream);
 }  // namespace tc
 
 // FP32-FMA (CUDA core) streaming kernel: the measured control.

@@ -26,7 +26,6 @@ __device__ __align__(256) float g_static_scratch[kScratchBytes / sizeof(float)];
 __device__ __align__(256) uint32_t g_static_status[64];
 
 constexpr int kMaxDevices = 64;
-constexpr int kEpiWarps = 8;
 
 // Per-device set-up, done once with that device current: the device
 // addresses of the two symbols (in host code the symbol names are host-side
@@ -62,7 +61,7 @@ void setup_device(DeviceSetup& s, int device) {
         s.status = (mhcpb_status_t)record_cuda_error(e, "cudaGetSymbolAddress (status word)");
         return;
     }
-    if ((e = tc::setup(false, kEpiWarps)) != cudaSuccess || (e = tc::setup(true, kEpiWarps)) != cudaSuccess) {
+    if ((e = tc::setup(false)) != cudaSuccess || (e = tc::setup(true)) != cudaSuccess) {
         s.status = (mhcpb_status_t)record_cuda_error(e, "setup (tensor-core kernel)");
         return;
     }
@@ -149,7 +148,7 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
     p.half_units = tc::use_half_units(items, s.sms) ? 1 : 0;
     const int grid = tc::grid_size(items, s.sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], grid, kEpiWarps, st)) != cudaSuccess)
+    if ((e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], grid, st)) != cudaSuccess)
         return (mhcpb_status_t)record_cuda_error(e, "launch (tensor-core kernel)");
     if ((e = launch_reduce(p.partial, dw, p.S, (int64_t)kNProj * K,
                            (flags & MHCPB_COMPENSATED_DW) != 0,

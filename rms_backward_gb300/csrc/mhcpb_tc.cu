@@ -57,11 +57,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDwCol = 256;                           // dW accumulators at 256 and 320
 constexpr uint32_t kDwColStride = 64;
 
-template <bool ADD, int NEPI>
+// Epilogue warps: one per (TMEM lane quarter, 64-column half of the strip).
+constexpr int NEPI = 8;
+
+template <bool ADD>
 struct Cfg {
     static constexpr int NS = ADD ? 2 : 4;                 // pipeline stages
     static constexpr int NP = 2;                           // split-P stages
-    static constexpr int HPW = 8 / NEPI;                   // 64-column boxes per epilogue warp
     static constexpr int threads = (4 + NEPI) * 32;
     // stage: X | raw P [128][24] | grad_r[128] | r[128] | addend (1 KiB-aligned parts)
     static constexpr uint32_t st_p = kXTile;
@@ -230,10 +232,10 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], float c, uint
     }
 }
 
-template <bool ADD, int NEPI>
-__global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
+template <bool ADD>
+__global__ void __launch_bounds__(Cfg<ADD>::threads, 1)
     main_tc_kernel(const MainParams p, const __grid_constant__ Maps maps) {
-    using C = Cfg<ADD, NEPI>;
+    using C = Cfg<ADD>;
     constexpr int NS = C::NS, NP = C::NP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
         // ------------------------------------------------------------ epilogue
         const int e = warp - 4;
         const int q = warp & 3;                  // TMEM lane quarter = token rows 32q..32q+31
-        const int h0 = (C::HPW == 2) ? 0 : e / 4;  // first 64-column box of this warp
+        const int h0 = e / 4;                    // the 64-column box of this warp
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int rr = q * 32 + lane;            // row within the token tile
         const float Kf = static_cast<float>(p.K);
@@ -577,8 +579,8 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
             // dW partial of this item: this warp's lanes are strip columns
             // 32q..32q+31 (TMEM lane quarter q), i.e. half q / 2 of the strip
             const bool cols_mine = ((I.hmask >> (q >> 1)) & 1u) != 0u;
-            const bool lo_part = cols_mine && ((C::HPW == 2) || h0 == 0);   // j 0..15
-            const bool hi_part = cols_mine && ((C::HPW == 2) || h0 == 1);   // j 16..23
+            const bool lo_part = cols_mine && h0 == 0;   // j 0..15
+            const bool hi_part = cols_mine && h0 == 1;   // j 16..23
             const uint32_t dcol = tmem + lane_base + kDwCol + (uint32_t)db * kDwColStride;
             uint32_t d0[16], d1[16], d2[16];
             // Stores this thread's columns of the partial (after the last tile's
@@ -632,7 +634,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     }
                     if (hi_part) ptx::tmem_ld_32x32b_x16(dcol + 32, d2);
                 }
-                const bool mine = (C::HPW == 2) ? (I.hmask != 0u) : (((I.hmask >> h0) & 1u) != 0u);
+                const bool mine = ((I.hmask >> h0) & 1u) != 0u;
                 if (!mine) {
                     // none of this warp's dX columns belong to this CTA in this item:
                     // only hand the accumulator(s) and the stage back
@@ -668,7 +670,7 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(bar(C::B_DE + db));
                 }
-                constexpr int nch = 2 * C::HPW;   // 32-column chunks of this warp
+                constexpr int nch = 2;   // 32-column chunks of this warp
 #pragma unroll
                 for (int ch = 0; ch < nch; ++ch) {
                     const int h = h0 + (ch >> 1);
@@ -733,34 +735,27 @@ __global__ void __launch_bounds__(Cfg<ADD, NEPI>::threads, 1)
     }
 }
 
-template <bool ADD, int NEPI>
+template <bool ADD>
 cudaError_t setup_one() {
-    return cudaFuncSetAttribute(main_tc_kernel<ADD, NEPI>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Cfg<ADD, NEPI>::alloc);
+    return cudaFuncSetAttribute(main_tc_kernel<ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Cfg<ADD>::alloc);
 }
 
-template <bool ADD, int NEPI>
+template <bool ADD>
 cudaError_t launch_one(const MainParams& p, const Maps& m, int grid, cudaStream_t stream) {
-    main_tc_kernel<ADD, NEPI><<<grid, Cfg<ADD, NEPI>::threads, Cfg<ADD, NEPI>::alloc, stream>>>(p, m);
+    main_tc_kernel<ADD><<<grid, Cfg<ADD>::threads, Cfg<ADD>::alloc, stream>>>(p, m);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t smem_bytes(bool has_addend, int epi_warps) {
-    if (epi_warps == 4) return has_addend ? Cfg<true, 4>::alloc : Cfg<false, 4>::alloc;
-    return has_addend ? Cfg<true, 8>::alloc : Cfg<false, 8>::alloc;
-}
+size_t smem_bytes(bool has_addend) { return has_addend ? Cfg<true>::alloc : Cfg<false>::alloc; }
 
-cudaError_t setup(bool has_addend, int epi_warps) {
-    if (epi_warps == 4) return has_addend ? setup_one<true, 4>() : setup_one<false, 4>();
-    return has_addend ? setup_one<true, 8>() : setup_one<false, 8>();
-}
+cudaError_t setup(bool has_addend) { return has_addend ? setup_one<true>() : setup_one<false>(); }
 
 cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensorMap& dx_map,
                    const CUtensorMap& add_map, const CUtensorMap& gp_map, const CUtensorMap& gr_map,
-                   const CUtensorMap& r_map, int grid, int epi_warps, cudaStream_t stream) {
+                   const CUtensorMap& r_map, int grid, cudaStream_t stream) {
     Maps m;
     m.x = x_map;
     m.dx = dx_map;
@@ -768,9 +763,7 @@ cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensor
     m.gp = gp_map;
     m.gr = gr_map;
     m.r = r_map;
-    const bool add = p.addend != nullptr;
-    if (epi_warps == 4) return add ? launch_one<true, 4>(p, m, grid, stream) : launch_one<false, 4>(p, m, grid, stream);
-    return add ? launch_one<true, 8>(p, m, grid, stream) : launch_one<false, 8>(p, m, grid, stream);
+    return p.addend != nullptr ? launch_one<true>(p, m, grid, stream) : launch_one<false>(p, m, grid, stream);
 }
 
 }  // namespace tc
