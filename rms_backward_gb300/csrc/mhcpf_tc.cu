@@ -55,11 +55,14 @@ constexpr uint32_t kWRawBox = kNProj * kBox * 4;       // 6 KiB: FP32 W rows x 6
 constexpr uint32_t kOffW = kNS * kBoxBytes;
 constexpr uint32_t kOffWRaw = kOffW + kBoxes * kWBoxBytes;
 constexpr uint32_t kOffBar = kOffWRaw + kBoxes * kWRawBox;
-// barriers: x_full[NS] x_empty[NS] acc_full[2] acc_empty[2] w_full w_empty fin w_raw
+// barriers: x_full[NS] x_empty[NS] acc_full[2] acc_empty[2] w_empty fin w_raw w_full[8]
 // (w_raw: a chunk of W as stored, FP32, landed by TMA; it is fetched one chunk
-// ahead, while the MMAs still use the previous chunk's converted W)
-constexpr int B_XF = 0, B_XE = kNS, B_AF = 2 * kNS, B_AE = 2 * kNS + 2, B_WF = 2 * kNS + 4,
-              B_WE = 2 * kNS + 5, B_FIN = 2 * kNS + 6, B_WR = 2 * kNS + 7, kBars = 2 * kNS + 8;
+// ahead, while the MMAs still use the previous chunk's converted W.  w_full[b]:
+// box b of the chunk converted, so the first MMAs of a chunk need not wait for
+// all eight boxes)
+constexpr int B_XF = 0, B_XE = kNS, B_AF = 2 * kNS, B_AE = 2 * kNS + 2, B_WE = 2 * kNS + 4,
+              B_FIN = 2 * kNS + 5, B_WR = 2 * kNS + 6, B_WF = 2 * kNS + 7,
+              kBars = 2 * kNS + 7 + kBoxes;
 constexpr uint32_t kOffMisc = kOffBar + kBars * 8;
 constexpr uint32_t kSmem = kOffMisc + 16 + 1024;        // + room to align the base to 1 KiB
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(B_AF + b), 1);
             ptx::mbar_init(bar(B_AE + b), 4);
         }
-        ptx::mbar_init(bar(B_WF), 2);
+        for (int b = 0; b < kBoxes; ++b) ptx::mbar_init(bar(B_WF + b), 2);
         ptx::mbar_init(bar(B_WE), 1);
         ptx::mbar_init(bar(B_FIN), 1);
         ptx::mbar_init(bar(B_WR), 1);
@@ -199,11 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int u = u_begin; u < u_end && ok; ++u) {
                 const Unit U = unit_at(p, u);
-                if (U.fc != prev_fc) {
-                    if (!wait_bar(bar(B_WF), (uint32_t)n_w & 1u, abort_flag, p.status, tmo, true)) {
-                        ok = false;
-                        break;
-                    }
+                const bool new_chunk = U.fc != prev_fc;   // W boxes: wait for each as it is needed
+                if (new_chunk) {
                     ++n_w;
                     prev_fc = U.fc;
                 }
@@ -213,7 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t d = tmem + (uint32_t)ab * 64u;
                 for (int b = 0; b < U.nb; ++b, ++n) {
-                    if (!wait_bar(bar(B_XF + st), ph, abort_flag, p.status, tmo, true)) {
+                    if ((new_chunk && !wait_bar(bar(B_WF + b), (uint32_t)(n_w - 1) & 1u, abort_flag,
+                                                p.status, tmo, true)) ||
+                        !wait_bar(bar(B_XF + st), ph, abort_flag, p.status, tmo, true)) {
                         ok = false;
                         break;
                     }
@@ -265,35 +267,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float4* raw = reinterpret_cast<const float4*>(smem + kOffWRaw);
             uint8_t* wsm = smem + kOffW;
-            // per box: 24 rows x 16 float4 = 384 float4, six per thread
+            for (int b = 0; b < kBoxes; ++b) {
+                // box b: 24 rows x 16 float4 = 384 float4, six per thread
 #pragma unroll 2
-            for (int i = tid; i < kBoxes * kNProj * (kBox / 4); i += 64) {
-                const int b = i / (kNProj * (kBox / 4));
-                const int rem = i - b * (kNProj * (kBox / 4));
-                const int j = rem >> 4, c4 = rem & 15;   // row, group of 4 columns
-                const float4 v4 = raw[i];
-                const float v[4] = {tf32_rna(v4.x), tf32_rna(v4.y), tf32_rna(v4.z), tf32_rna(v4.w)};
-                uint32_t hi[2], lo[2];
+                for (int k = 0; k < kNProj * (kBox / 4) / 64; ++k) {
+                    const int rem = tid + 64 * k;
+                    const int j = rem >> 4, c4 = rem & 15;   // row, group of 4 columns
+                    const float4 v4 = raw[b * (kNProj * (kBox / 4)) + rem];
+                    const float v[4] = {tf32_rna(v4.x), tf32_rna(v4.y), tf32_rna(v4.z), tf32_rna(v4.w)};
+                    uint32_t hi[2], lo[2];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-                    hi[e] = *reinterpret_cast<const uint32_t*>(&h);
-                    const float r0 = isfinite(v[2 * e]) ? v[2 * e] - __low2float(h) : 0.f;
-                    const float r1 = isfinite(v[2 * e + 1]) ? v[2 * e + 1] - __high2float(h) : 0.f;
-                    const __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
-                    lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+                    for (int e = 0; e < 2; ++e) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                        hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+                        const float r0 = isfinite(v[2 * e]) ? v[2 * e] - __low2float(h) : 0.f;
+                        const float r1 = isfinite(v[2 * e + 1]) ? v[2 * e + 1] - __high2float(h) : 0.f;
+                        const __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+                        lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+                    }
+                    // 128-byte swizzle: 16-byte chunk c of row n sits at chunk c ^ (n & 7);
+                    // four columns are 8 bytes, half a chunk
+                    uint8_t* box = wsm + b * kWBoxBytes;
+                    const int c16 = c4 >> 1, half = (c4 & 1) * 8;
+                    const int nh = j, nl = kNProj + j;
+                    *reinterpret_cast<uint2*>(box + nh * 128 + ((c16 ^ (nh & 7)) << 4) + half) = make_uint2(hi[0], hi[1]);
+                    *reinterpret_cast<uint2*>(box + nl * 128 + ((c16 ^ (nl & 7)) << 4) + half) = make_uint2(lo[0], lo[1]);
                 }
-                // 128-byte swizzle: 16-byte chunk c of row n sits at chunk c ^ (n & 7);
-                // four columns are 8 bytes, half a chunk
-                uint8_t* box = wsm + b * kWBoxBytes;
-                const int c16 = c4 >> 1, half = (c4 & 1) * 8;
-                const int nh = j, nl = kNProj + j;
-                *reinterpret_cast<uint2*>(box + nh * 128 + ((c16 ^ (nh & 7)) << 4) + half) = make_uint2(hi[0], hi[1]);
-                *reinterpret_cast<uint2*>(box + nl * 128 + ((c16 ^ (nl & 7)) << 4) + half) = make_uint2(lo[0], lo[1]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(B_WF + b));
             }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(B_WF));
             if (fetcher) FTRACE(F_W_READY, n_w);
             ++n_w;
             // the raw buffer is free once both warps have converted it: fetch the
@@ -304,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (f != U.fc) { next_fc = f; break; }
             }
             if (fetcher && next_fc >= 0) {
-                if (!wait_bar(bar(B_WF), (uint32_t)(n_w - 1) & 1u, abort_flag, p.status, tmo, true)) {
+                // both warps have converted the last box, hence every box
+                if (!wait_bar(bar(B_WF + kBoxes - 1), (uint32_t)(n_w - 1) & 1u, abort_flag, p.status,
+                              tmo, true)) {
                     ok = false;
                 } else {
                     fetch_raw_w(next_fc);
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // summed squares.  Thread = (partial row j' in 0..24, token t); a warp reads
 // 128 contiguous bytes of a chunk's row per load.
 constexpr int kReduceThreads = 256;
-constexpr int kGroup = 20;   // chunk partials loaded before they are summed
+constexpr int kGroup = 40;   // chunk partials loaded before they are summed (all of them at K = 20480)
 
 __global__ void __launch_bounds__(kReduceThreads)
     fwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ proj,
