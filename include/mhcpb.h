@@ -259,7 +259,7 @@ mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uint32_t flags
                                             const void* grad_x_addend, void* stream);
 
 /* ---------------------------------------------------------------------------
- * The forward of the stage (SURVEY "next" row: the step before the backward).
+ * The forward of the stage (the step before the backward in the graph).
  * The prime-kernels PR #15 page describes its mhc_projection as the RMS of the
  * streams and the projection logits in one read of the streams; this stage's
  * backward (the cuDNN page above) receives the gradients of exactly these two
