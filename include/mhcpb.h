@@ -10,15 +10,15 @@
  *
  * Both matrix products use operands converted to TF32 (round to nearest,
  * ties away) with FP32 accumulation; the RMS term is FP32 arithmetic.  dW is
- * reduced over tokens in a fixed order without atomics, so it is bitwise
+ * summed over tokens in an order fixed in advance and with no atomic adds, so it is bitwise
  * reproducible for a given (T, K) on any GB300.  Outputs are overwritten,
- * never accumulated into.  The last 8 columns of grad_proj are never read.
+ * never accumulated into.  grad_proj's columns 24..31 are not read at all.
  *
  * The caller-facing shape of the API follows the same page's "Prepared class
  * API": a plan is created once per shape, reports its scratch size, and each
- * execute enqueues exactly two kernels on the caller's stream (a streaming
- * kernel that writes dX and per-chunk dW partials into the workspace, then a
- * fixed-order reduction of the partials into dW) and allocates nothing.
+ * execute launches two kernels on the caller's stream (a streaming kernel
+ * that writes dX and per-chunk dW partials into the workspace, then a
+ * fixed-order reduction of the partials into dW) and makes no allocation.
  *
  * Layouts (all compact row-major, the page's "Requirements and tensor
  * contract"):
@@ -106,8 +106,8 @@ enum {
      * dW_out = dW_in + D in FP32 (one rounding), where D is exactly what the
      * execute would write without this flag (plain or compensated).  For
      * callers that sum weight gradients over micro-batches in an FP32 buffer of
-     * their own (the pages' "accumulate FP8 weight gradients straight into a
-     * caller's fp32 buffer", prime-kernels PR #15, applied here to dW).  dW must
+     * their own (prime-kernels PR #15 offers this for its FP8 expert weight
+     * gradients; here it applies to dW).  dW must
      * then hold valid values before the execute; dX is unaffected. */
     MHCPB_ACCUMULATE_DW = 16u,
     /* Test hook for failure detection: in the tensor-core kernel the MMA
@@ -158,7 +158,7 @@ mhcpb_status_t mhcpb_execute(mhcpb_plan_t plan,
 
 /* The same backward in two calls, so that a caller can start using dX (send
  * it, or run the next layer's backward) before dW exists -- the split
- * backward of the prime-kernels PR #15 ("data gradient first, weight
+ * backward of the prime-kernels PR #15 (input gradient before the weight
  * gradients after"), applied to this stage:
  *
  *   mhcpb_execute_dx: enqueues the streaming kernel only.  When it completes,
@@ -261,7 +261,7 @@ mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uint32_t flags
 /* ---------------------------------------------------------------------------
  * The forward of the stage (the step before the backward in the graph).
  * The prime-kernels PR #15 page describes its mhc_projection as the RMS of the
- * streams and the projection logits in one read of the streams; this stage's
+ * streams and the projection logits, both from a single pass over X; this stage's
  * backward (the cuDNN page above) receives the gradients of exactly these two
  * outputs, and its dX formula is their vector-Jacobian product:
  *

@@ -12,7 +12,7 @@ intro):
     dW = P.T @ X
 
 Precision contract from the same passage: both matrix products take operands
-converted to TF32 and accumulate in FP32; the RMS term is FP32 arithmetic; dX is
+rounded to TF32 with FP32 sums; the RMS term is computed in FP32; dX is
 stored BF16 and dW FP32.  The oracle evaluates the exact value of that
 definition in FP64 over the TF32-rounded product operands (X is BF16, a subset
 of TF32, so it needs no rounding), then rounds once: dX to BF16

@@ -6,7 +6,7 @@ here is shared with the CUDA path.
 
 What the forward computes.  The prime-kernels PR #15 page describes its
 ``mhc_projection`` as the RMS of the streams and the projection (gate) logits
-computed in one read of the streams; the cuDNN frontend page "DSv4.1 mHC
+from a single pass over the streams; the cuDNN frontend page "DSv4.1 mHC
 projection/RMS backward" (intro) fixes what the backward of this stage
 receives: the gradient of a [T, 32] projection output of which the first 24
 columns are used, and the gradient of a per-row RMS r[T].  Its formula,
@@ -18,7 +18,7 @@ dX = P @ W + grad_r / (r * K) * X, is exactly the vector-Jacobian product of
 so these are the forward this oracle defines (the plainest reading; the
 pages give no formula for the forward itself).  The output layout mirrors the
 backward's input: proj is FP32 [T, 32] with columns 24..31 written as zero,
-r is FP32 [T].  The "collapse of the streams" that the PR also fuses into its
+r is FP32 [T].  The stream collapse that the PR also fuses into its
 forward needs the previous sublayer's weights, which the pages do not define;
 it is not part of this stage.
 

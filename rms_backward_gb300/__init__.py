@@ -55,7 +55,7 @@ class Plan:
 
     def execute(self, x, w, grad_proj, grad_r, r, dx, dw, workspace, addend=None, stream=None):
         """Enqueue on ``stream`` (a torch.cuda.Stream, a raw handle, or None for
-        the current stream of the tensors' device)."""
+        the device's current stream)."""
         if stream is None:
             import torch
             stream = torch.cuda.current_stream(x.device).cuda_stream

@@ -2,7 +2,7 @@
 // tensor contract checks of the cuDNN frontend page "DSv4.1 mHC
 // projection/RMS backward" ("Requirements and tensor contract"), TMA tensor
 // map encoding and the two launches of one execute ("Prepared class API":
-// execute enqueues exactly two kernels and allocates nothing).
+// each execute launches the two kernels and allocates no memory).
 #include <cuda.h>
 #include <cuda_runtime.h>
 

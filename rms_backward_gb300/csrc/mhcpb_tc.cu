@@ -11,7 +11,7 @@
 //  * The grid is persistent (one CTA per SM).  Work items are (128-column
 //    strip, token chunk) pairs in strip-major order; a CTA takes a contiguous
 //    range of them, so W for a strip is staged once per strip.  The chunking
-//    depends only on T, so dW bits do not depend on the SM count.
+//    depends only on T, so dW bits are the same on every SM count.
 //  * One pipeline stage per 128-token tile, filled by TMA: the X tile
 //    (128 x 128 BF16 as two 64-column boxes, 128-byte swizzle, read from HBM
 //    exactly once, L2 evict-first), the tile's 24 used grad_proj columns and

@@ -4,7 +4,7 @@
 //   r[t]       = sqrt(sum_k X[t, k]^2 / K + eps)
 //
 // The prime-kernels PR #15 page describes its mhc_projection as the RMS and
-// the projection logits computed in one read of the streams; the backward
+// the projection logits, both from a single pass over X; the backward
 // of this stage (cuDNN frontend page "DSv4.1 mHC projection/RMS backward",
 // intro) takes the gradients of exactly these two outputs (its dX formula is
 // their vector-Jacobian product).  proj is written FP32 [T, 32] with columns

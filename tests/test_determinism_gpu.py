@@ -103,7 +103,7 @@ def test_independent_plans_same_shape_agree():
 def test_bitwise_independent_of_grid_size(T, K):
     """The dW partition depends only on T: capping the persistent grid at any
     number of CTAs (which moves where items are split between CTAs) leaves dX
-    and dW bitwise unchanged, so results do not depend on the SM count."""
+    and dW bitwise unchanged: the same bits on every SM count."""
     wl = WL.make("grid", T=T, K=K, seed=34)
     r = Runner(wl)
     full = r.plan.query("grid")

@@ -2,7 +2,7 @@
 (oracle/mhcpf_oracle.py): proj = X W^T over TF32 W and r = sqrt(mean X^2 +
 eps), the two outputs whose gradients the backward receives (cuDNN frontend
 page "DSv4.1 mHC projection/RMS backward", intro; the prime-kernels PR #15
-page's mhc_projection computes them in one read of the streams)."""
+page's mhc_projection computes both from a single pass over X)."""
 import numpy as np
 import pytest
 import torch

@@ -1,9 +1,9 @@
 """Split backward (mhcpb_execute_dx + mhcpb_reduce_dw) and accumulation of dW
 into the caller's buffer (MHCPB_ACCUMULATE_DW).
 
-The split follows the prime-kernels PR #15 "split backward ops" (data
-gradient first, weight gradients after); the accumulation follows its
-"accumulate weight gradients straight into a caller's fp32 buffer".  Both must
+The split follows the split backward of the prime-kernels PR #15 (the input
+gradient is produced before the weight gradients); the accumulation follows
+its option of adding weight gradients into an FP32 buffer the caller owns.  Both must
 leave the arithmetic unchanged: the split gives mhcpb_execute's bits, and an
 accumulating execute gives exactly fp32(dW_in + D) with D the bits the
 non-accumulating execute writes.
