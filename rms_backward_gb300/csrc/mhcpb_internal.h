@@ -43,7 +43,7 @@ struct MainParams {
 
 // Timeline stamps of a traced build: [grid][kTraceEvents][kTraceTiles] u64.
 constexpr int kTraceEvents = 19;
-constexpr int kTraceTiles = 48;
+constexpr int kTraceTiles = 80;
 
 constexpr uint32_t kTestInjectStall = 1u;
 
