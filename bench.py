@@ -159,23 +159,44 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle timing
+class _CpuClock:
+    """Wall time and process CPU time (all threads) over the timed oracle calls;
+    their ratio is the number of cores the oracle actually kept busy."""
+
+    def __init__(self):
+        self.wall = 0.0
+        self.cpu = 0.0
+
+    def __enter__(self):
+        self._w, self._c = time.perf_counter(), time.process_time()
+        return self
+
+    def __exit__(self, *exc):
+        self.wall += time.perf_counter() - self._w
+        self.cpu += time.process_time() - self._c
+
+    def cores(self):
+        return round(self.cpu / self.wall, 1) if self.wall > 0 else 1.0
+
+
 def _oracle_rate(wl_full_T, K, seconds, seed=1):
     """Runs the CPU oracle on 512-token slices of the training-profile workload
-    until about `seconds` have passed; returns (GB/s-equivalent, tokens, secs)."""
+    until about `seconds` have passed; returns (GB/s-equivalent, tokens, secs,
+    cores kept busy)."""
     sys.path.insert(0, ROOT)
     import oracle.mhcpb_oracle as O
-    done_tokens, elapsed, nbytes = 0, 0.0, 0
+    done_tokens, nbytes = 0, 0
     piece = 512
     i = 0
-    while elapsed < seconds and done_tokens < wl_full_T:
+    clock = _CpuClock()
+    while clock.wall < seconds and done_tokens < wl_full_T:
         wl = WL.make("cpu_sample", T=piece, K=K, seed=seed + 1000 * i)
-        t0 = time.perf_counter()
-        O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
-        elapsed += time.perf_counter() - t0
+        with clock:
+            O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
         done_tokens += piece
         nbytes += WL.algorithmic_bytes(piece, K)
         i += 1
-    return nbytes / elapsed / 1e9, done_tokens, elapsed
+    return nbytes / clock.wall / 1e9, done_tokens, clock.wall, clock.cores()
 
 
 def _cpu_threads():
@@ -187,7 +208,7 @@ def _cpu_threads():
             return int(max(blas))
     except Exception:
         pass
-    return os.cpu_count() or 1
+    return None   # not known without threadpoolctl
 
 
 def run_reference(args):
@@ -209,12 +230,13 @@ def run_reference(args):
     wl = WL.make("ref_step", T=tok, K=K, seed=78)
     for _ in range(args.warmup):
         O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
-    secs = time.perf_counter() - t0
+    clock = _CpuClock()
+    with clock:
+        for _ in range(args.steps):
+            O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
+    secs = clock.wall
     gbs = WL.algorithmic_bytes(tok, K) * args.steps / secs / 1e9
-    cores = _cpu_threads()
+    cores = clock.cores()
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup,
@@ -223,6 +245,7 @@ def run_reference(args):
         "config": {"workload": f"training profile T={T} K={K} (4 streams x hidden 5120)",
                    "T": T, "K": K, "sample_tokens_per_step": tok},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "cores_available": os.cpu_count(), "blas_threads": _cpu_threads(),
                          "sample": f"{tok} tokens x K={K} of the training profile per step"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -409,8 +432,9 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
-        gbs, toks, secs = _oracle_rate(T, K, seconds=12.0)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": _cpu_threads(), "kind": "oracle",
+        gbs, toks, secs, cores = _oracle_rate(T, K, seconds=12.0)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "cores_available": os.cpu_count(), "blas_threads": _cpu_threads(),
                "sample": f"{toks} of {T} tokens x K={K} of the training profile "
                          f"(512-token slices, {secs:.1f} s)"}
 
@@ -576,16 +600,18 @@ def run_forward(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle.mhcpf_oracle as F
-        done, secs, nbytes, i = 0, 0.0, 0, 0
-        while secs < 10.0 and done < T:
+        done, nbytes, i = 0, 0, 0
+        clock = _CpuClock()
+        while clock.wall < 10.0 and done < T:
             piece = WL.make("cpu_sample", T=256, K=K, seed=cfg["seed"] + 1000 * i)
-            t0 = time.perf_counter()
-            F.mhc_proj_forward(piece.x, piece.w)
-            secs += time.perf_counter() - t0
+            with clock:
+                F.mhc_proj_forward(piece.x, piece.w)
             done += 256
             nbytes += WL.algorithmic_bytes_forward(256, K)
             i += 1
-        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": _cpu_threads(), "kind": "oracle",
+        secs = clock.wall
+        cpu = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": clock.cores(), "kind": "oracle",
+               "cores_available": os.cpu_count(), "blas_threads": _cpu_threads(),
                "sample": f"{done} of {T} tokens x K={K} (256-token slices, {secs:.1f} s)"}
 
     if rank == 0:
