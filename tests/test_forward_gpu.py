@@ -150,3 +150,40 @@ def test_forward_rejections_write_nothing():
     torch.cuda.synchronize()
     assert bool((proj == 7.0).all()) and bool((r == 7.0).all())
     plan.close()
+
+
+def test_graph_capture_replay_and_new_inputs():
+    """Captured once into a CUDA graph on a side stream, the forward replays
+    with the same bits, and picks up new contents of the captured buffers."""
+    wl = WL.make("fg", T=1000, K=1032, seed=77)
+    wl2 = WL.make("fg2", T=1000, K=1032, seed=78)
+    ref_p, ref_r = run_forward(wl)
+    ref2_p, ref2_r = run_forward(wl2)
+    plan = Plan(wl.T, wl.K, 0)
+    x = torch.from_numpy(wl.x.view(np.int16)).view(torch.bfloat16).to(DEV)
+    w = torch.from_numpy(wl.w).to(DEV)
+    proj = torch.full((wl.T, 32), float("nan"), device=DEV)
+    r = torch.full((wl.T,), float("nan"), device=DEV)
+    ws = torch.full((plan.forward_workspace_bytes // 4,), float("nan"), device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            plan.forward(x, w, proj, r, ws, stream=s)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        proj.fill_(float("nan"))
+        r.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(proj.cpu().numpy().view(np.uint32), ref_p.view(np.uint32))
+        assert np.array_equal(r.cpu().numpy().view(np.uint32), ref_r.view(np.uint32))
+    x.copy_(torch.from_numpy(wl2.x.view(np.int16)).view(torch.bfloat16))
+    w.copy_(torch.from_numpy(wl2.w))
+    g.replay()
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    assert np.array_equal(proj.cpu().numpy().view(np.uint32), ref2_p.view(np.uint32))
+    assert np.array_equal(r.cpu().numpy().view(np.uint32), ref2_r.view(np.uint32))
+    plan.close()
