@@ -122,3 +122,37 @@ def test_bitwise_independent_of_grid_size(T, K):
     r.plan.set_max_ctas(0)
     assert r.plan.query("grid") == full
     r.plan.close()
+
+
+def test_one_plan_overlapping_executes_on_two_streams():
+    """One plan, two streams, separate inputs, outputs and workspaces, launched
+    back to back without ordering between the streams (the contract allows
+    overlapping executions that do not share buffers): each stream's results
+    equal that input's serial results bit for bit."""
+    wa = WL.make("ovl_a", T=1500, K=2048, seed=33)
+    wb = WL.make("ovl_b", T=1500, K=2048, seed=34)
+    ra, rb = Runner(wa), Runner(wb)
+    ra.run()
+    rb.run()
+    ref_a, ref_b = _bits(ra), _bits(rb)
+    plan = ra.plan                       # rb's buffers driven through ra's plan
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    for r in (ra, rb):
+        r.dx.fill_(float("nan"))
+        r.dw.fill_(float("nan"))
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for r, s in ((ra, sa), (rb, sb)):
+            i = r.inp
+            plan.execute(i["x"], i["w"], i["grad_proj"], i["grad_r"], i["r"], r.dx, r.dw, r.ws,
+                         stream=s)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    for r, ref in ((ra, ref_a), (rb, ref_b)):
+        dx = r.dx.view(torch.int16).cpu().numpy().view(np.uint16)
+        dw = r.dw.cpu().numpy().view(np.uint32)
+        assert np.array_equal(dx, ref[0]) and np.array_equal(dw, ref[1])
+    ra.plan.close()
+    rb.plan.close()
