@@ -146,3 +146,23 @@ def test_tolerance_checks_accept_self_and_reject_perturbation():
     assert not F.check_proj(bad, proj, bound)[0]
     assert F.check_r(r.astype(np.float32), r)[0]
     assert not F.check_r((r * (1 + 2 ** -12)).astype(np.float32), r)[0]
+
+
+def test_forward_oracle_reproduces_frozen_fixture():
+    """tests/golden/forward_T8_K16.txt holds the forward oracle's output (rounded
+    to FP32) on a fixed seeded workload, written by tests/golden/make_golden.py:
+    a later change to the oracle's arithmetic shows up here."""
+    import os
+
+    from rms_backward_gb300 import workloads as WL
+    path = os.path.join(os.path.dirname(__file__), "golden", "forward_T8_K16.txt")
+    rec = {}
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        key, *vals = line.split()
+        rec[key] = np.array([int(v, 16) for v in vals], dtype=np.uint32)
+    wl = WL.make("golden", T=8, K=16, seed=1234, addend=True)
+    proj, r = F.mhc_proj_forward(wl.x, wl.w)
+    assert np.array_equal(proj.astype(np.float32).view(np.uint32).reshape(-1), rec["proj"])
+    assert np.array_equal(r.astype(np.float32).view(np.uint32).reshape(-1), rec["r"])
