@@ -254,14 +254,17 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
+# the sources the streaming (tensor-core) kernel is compiled from
+_STREAMING_KERNEL_SOURCES = ("mhcpb_internal.h", "mhcpb_tc.cu", "mhcpb_wait.cuh", "ptx.cuh")
+
+
 def _kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rms_backward_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in _STREAMING_KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
