@@ -10,7 +10,8 @@ import pytest
 
 from rms_backward_gb300 import abi
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mhcpb.h")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mhcpb.h")
 
 
 def _built():
@@ -88,3 +89,18 @@ def test_workspace_formula_matches_page_size():
     T, K = 4096, 20480
     S = -(-T // abi.MHCPB_PARTIAL_TOKENS(T))
     assert S * 24 * K * 4 == 15_728_640
+
+
+def test_missing_library_fails_loudly():
+    """No CPU fallback: without the built library the binding raises (run in a
+    fresh interpreter so the already loaded library is not reused)."""
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from rms_backward_gb300 import abi\n"
+            "try:\n"
+            "    abi.load('/nonexistent/libmhcpb.so')\n"
+            "except RuntimeError as e:\n"
+            "    print('raised', 'missing' in str(e))\n" % ROOT)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert out.stdout.strip() == "raised True", out.stdout + out.stderr
