@@ -50,6 +50,9 @@ template <bool COMP, bool ACC>
 __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4* __restrict__ part,
                                                                    float4* __restrict__ dw, int S,
                                                                    int64_t n4, int discard) {
+    // the next execute's streaming kernel may be scheduled now; it waits for
+    // this grid's completion before it touches global memory
+    ptx::grid_launch_dependents();
     ptx::grid_dependency_wait();
     const int64_t i = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x;
     const bool valid = i < n4;   // n4 % 8 == 0: a 128-byte line is all valid or all not

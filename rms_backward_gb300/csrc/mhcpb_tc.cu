@@ -311,6 +311,10 @@ __global__ void __launch_bounds__(Cfg<ADD>::threads, 1)
         ptx::prefetch_tensormap(&maps.gr);
         ptx::prefetch_tensormap(&maps.r);
         if (ADD) ptx::prefetch_tensormap(&maps.add);
+        // Launched as a programmatic dependent: everything above touches only
+        // shared memory and the kernel parameters; no global memory is read or
+        // written before the grids this one depends on have completed.
+        ptx::grid_dependency_wait();
         // Fill every stage now (all start empty), so the first loads overlap
         // the TMEM allocation and the block-wide sync below.
         const uint64_t pol_stream = ptx::policy_evict_first();
@@ -329,6 +333,7 @@ __global__ void __launch_bounds__(Cfg<ADD>::threads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    ptx::grid_dependency_wait();   // (returns at once: thread 0 waited above)
     ptx::grid_launch_dependents();
 
     const uint64_t tmo = p.timeout_ns;
@@ -743,8 +748,20 @@ cudaError_t setup_one() {
 
 template <bool ADD>
 cudaError_t launch_one(const MainParams& p, const Maps& m, int grid, cudaStream_t stream) {
-    main_tc_kernel<ADD><<<grid, Cfg<ADD>::threads, Cfg<ADD>::alloc, stream>>>(p, m);
-    return cudaGetLastError();
+    // programmatic dependent launch: the CTAs may be scheduled while the
+    // previous kernel in the stream (e.g. the reduction of a previous
+    // execute) finishes; they wait for it before touching global memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(Cfg<ADD>::threads);
+    cfg.dynamicSmemBytes = Cfg<ADD>::alloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, main_tc_kernel<ADD>, p, m);
 }
 
 }  // namespace

@@ -154,6 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&xmap);
         ptx::prefetch_tensormap(&wmap);
+        // Launched as a programmatic dependent: no global memory is touched
+        // before the grids this one depends on have completed.
+        ptx::grid_dependency_wait();
         // the first chunk of W goes out before any X load: the MMAs cannot start
         // (nor release a stage) before it is converted
         if (u_begin < u_end) fetch_raw_w(unit_at(p, u_begin).fc);
@@ -166,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    ptx::grid_dependency_wait();   // (returns at once: thread 0 waited above)
     ptx::grid_launch_dependents();
 
     if (warp == 0) {
@@ -433,6 +437,7 @@ __global__ void __launch_bounds__(kReduceThreads)
     fwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ proj,
                       float* __restrict__ r, int T, int t_pad, int n_fc, float kf, float eps,
                       int discard) {
+    ptx::grid_launch_dependents();   // the next forward's kernel 1 may be scheduled
     ptx::grid_dependency_wait();
     const int64_t i = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x;
     const bool valid = i < (int64_t)kPartRows * t_pad;   // t_pad % 32 == 0: whole warps
@@ -480,8 +485,20 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorM
                    cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, cudaEvent_t ev2) {
     cudaError_t e;
     if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return e;
-    fwd_tc_kernel<<<grid, kThreads, kSmem, stream>>>(p, x_map, w_map);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
+        // programmatic dependent launch, as for the backward's streaming kernel
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, fwd_tc_kernel, p, x_map, w_map)) != cudaSuccess) return e;
+    }
     if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return e;
     const int64_t n = (int64_t)kPartRows * p.t_pad;
     // discard needs 128-byte lines: t_pad is a multiple of 32 floats
