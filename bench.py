@@ -6,8 +6,11 @@ One step = one backward (both kernels) over the training-profile workload
 already resident in HBM.  The metric is achieved HBM bandwidth: algorithmic
 bytes (read X, write dX, read W, write dW, read the 24 used grad_proj columns,
 read r and grad_r) divided by the step time measured with CUDA events on the
-launching stream; L2 is flushed (a 256 MiB write) before every timed step,
-outside the timed interval.  Prints one JSON line.
+launching stream.  When the step's inputs are larger than L2 the K steps run
+back to back between one pair of events (no flush needed: nothing useful stays
+in L2); otherwise L2 is flushed (a 256 MiB write) before every step, outside
+events around each step.  The flushed per-step timing is also reported in the
+first case (`flushed`).  Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
