@@ -148,7 +148,10 @@ mhcpb_status_t mhcpb_workspace_bytes(mhcpb_plan_t plan, size_t* bytes);
  * 16-byte aligned and pairwise disjoint; `grad_x_addend` must be NULL unless
  * the plan has MHCPB_HAS_ADDEND, and non-NULL if it has.  Returns without
  * synchronising.  Capturable into a CUDA graph (no allocation, no host sync;
- * tensor maps travel by value in the kernel parameters). */
+ * tensor maps travel by value in the kernel parameters).  Both kernels are
+ * launched as programmatic dependents of the kernel before them in the
+ * stream: they may be scheduled early but touch no global memory before it
+ * has completed, so stream order holds as for ordinary launches. */
 mhcpb_status_t mhcpb_execute(mhcpb_plan_t plan,
                              const void* x, const float* w, const float* grad_proj,
                              const float* grad_r, const float* r,
@@ -158,8 +161,8 @@ mhcpb_status_t mhcpb_execute(mhcpb_plan_t plan,
 
 /* The same backward in two calls, so that a caller can start using dX (send
  * it, or run the next layer's backward) before dW exists -- the split
- * backward of the prime-kernels PR #15 (input gradient before the weight
- * gradients after"), applied to this stage:
+ * backward of the prime-kernels PR #15 (the input gradient first, the weight
+ * gradients after), applied to this stage:
  *
  *   mhcpb_execute_dx: enqueues the streaming kernel only.  When it completes,
  *   dX is final and `workspace` holds the dW partials of these inputs.
