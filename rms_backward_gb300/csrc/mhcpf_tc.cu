@@ -26,9 +26,12 @@
 //    the TF32 product), is the K-major B operand [Wh; Wl] (N = 48).  The
 //    unit's 8 boxes accumulate into one TMEM accumulator (double-buffered
 //    across units); proj = D[:, j] + D[:, 24 + j];
-//  * warps 2-3: W preparation: each chunk of W is fetched by TMA (FP32, one
-//    chunk ahead) and converted in shared memory (TF32 rounding, hi/lo split,
-//    128-byte-swizzled K-major layout);
+//  * warps 2-3: W preparation: each chunk of W is fetched by TMA (FP32) into
+//    one of two W slots and converted there in place (TF32 rounding, hi/lo
+//    split, 128-byte-swizzled K-major layout; a 64-column box is 6 KiB in
+//    either form), so a CTA whose units span two chunks converts the second
+//    while the MMAs still use the first (one slot converted after the first
+//    chunk's MMAs: 41.2 us for this kernel; two slots: 39.7 us);
 //  * warps 4-7: per token row, the sum of squares of the X box from shared
 //    memory (eight 8-term partial sums, then their sum: a shallow FP32 sum),
 //    and at the end of each unit the drain of the accumulator; they write
@@ -58,17 +61,17 @@ constexpr int kNS = 2;                                 // X pipeline stages
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 128;                    // two accumulators of 64 columns
 constexpr uint32_t kWRawBox = kNProj * kBox * 4;       // 6 KiB: FP32 W rows x 64 columns
-constexpr uint32_t kOffW = kNS * kStageBytes;
-constexpr uint32_t kOffWRaw = kOffW + kBoxes * kWBoxBytes;
-constexpr uint32_t kOffBar = kOffWRaw + kBoxes * kWRawBox;
-// barriers: x_full[NS] x_empty[NS] acc_full[2] acc_empty[2] w_empty fin w_raw w_full[8]
-// (w_raw: a chunk of W as stored, FP32, landed by TMA; it is fetched one chunk
-// ahead, while the MMAs still use the previous chunk's converted W.  w_full[b]:
-// box b of the chunk converted, so the first MMAs of a chunk need not wait for
-// all eight boxes)
+static_assert(kWRawBox == kWBoxBytes, "a W box is converted in place");
+constexpr uint32_t kWSlot = kBoxes * kWBoxBytes;       // 48 KiB: one chunk of W
+constexpr uint32_t kOffW = kNS * kStageBytes;          // two W slots
+constexpr uint32_t kOffBar = kOffW + 2 * kWSlot;
+// barriers: x_full[NS] x_empty[NS] acc_full[2] acc_empty[2] w_empty[2] fin w_raw[2] w_full[2][8]
+// (per W slot: w_raw, the chunk as stored (FP32) landed by TMA; w_full[b], box
+// b converted in place, so the first MMAs of a chunk need not wait for all
+// eight boxes; w_empty, the MMAs done with the slot)
 constexpr int B_XF = 0, B_XE = kNS, B_AF = 2 * kNS, B_AE = 2 * kNS + 2, B_WE = 2 * kNS + 4,
-              B_FIN = 2 * kNS + 5, B_WR = 2 * kNS + 6, B_WF = 2 * kNS + 7,
-              kBars = 2 * kNS + 7 + kBoxes;
+              B_FIN = 2 * kNS + 6, B_WR = 2 * kNS + 7, B_WF = 2 * kNS + 9,
+              kBars = 2 * kNS + 9 + 2 * kBoxes;
 constexpr uint32_t kOffMisc = kOffBar + kBars * 8;
 constexpr uint32_t kSmem = kOffMisc + 16 + 1024;        // + room to align the base to 1 KiB
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -127,13 +130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int u_end = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
     const uint64_t tmo = p.timeout_ns;
     // one chunk of W as stored (eight 64-column FP32 boxes, zero past K) into
-    // the raw buffer, L2 evict-last: every token tile re-reads W
-    auto fetch_raw_w = [&](int fc) {
+    // W slot `slot`, L2 evict-last: every token tile re-reads W
+    auto fetch_raw_w = [&](int fc, int slot) {
         const uint64_t pol_keep = ptx::policy_evict_last();
-        ptx::mbar_arrive_expect_tx(bar(B_WR), kBoxes * kWRawBox);
+        ptx::mbar_arrive_expect_tx(bar(B_WR + slot), kBoxes * kWRawBox);
         for (int b = 0; b < kBoxes; ++b)
-            ptx::tma_load_2d(sbase + kOffWRaw + (uint32_t)b * kWRawBox, &wmap, fc * kChunk + b * kBox,
-                             0, bar(B_WR), pol_keep);
+            ptx::tma_load_2d(sbase + kOffW + (uint32_t)slot * kWSlot + (uint32_t)b * kWRawBox, &wmap,
+                             fc * kChunk + b * kBox, 0, bar(B_WR + slot), pol_keep);
     };
 
     if (threadIdx.x == 0) {
@@ -146,10 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(B_AF + b), 1);
             ptx::mbar_init(bar(B_AE + b), 4);
         }
-        for (int b = 0; b < kBoxes; ++b) ptx::mbar_init(bar(B_WF + b), 2);
-        ptx::mbar_init(bar(B_WE), 1);
+        for (int b = 0; b < 2 * kBoxes; ++b) ptx::mbar_init(bar(B_WF + b), 1);   // the converting warp
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(bar(B_WE + s), 1);
+            ptx::mbar_init(bar(B_WR + s), 1);
+        }
         ptx::mbar_init(bar(B_FIN), 1);
-        ptx::mbar_init(bar(B_WR), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&xmap);
@@ -159,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::grid_dependency_wait();
         // the first chunk of W goes out before any X load: the MMAs cannot start
         // (nor release a stage) before it is converted
-        if (u_begin < u_end) fetch_raw_w(unit_at(p, u_begin).fc);
+        if (u_begin < u_end) fetch_raw_w(unit_at(p, u_begin).fc, 0);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_holder), kTmemCols);
@@ -208,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 48, false, false);
-            const uint32_t w_base = sbase + kOffW;
             int st = 0, ab = 0, n_w = 0, prev_fc = -1, n = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
@@ -224,11 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t d = tmem + (uint32_t)ab * 64u;
+                const int wslot = (n_w - 1) & 1;   // chunk m of this CTA sits in slot m % 2
+                const uint32_t w_base = sbase + kOffW + (uint32_t)wslot * kWSlot;
                 for (int b = 0; b < U.nb; b += kBPS, ++n) {
                     const int nbx = min(kBPS, U.nb - b);
                     for (int i = 0; i < nbx && ok; ++i)
-                        if (new_chunk && !wait_bar(bar(B_WF + b + i), (uint32_t)(n_w - 1) & 1u, abort_flag,
-                                                   p.status, tmo, true))
+                        if (new_chunk && !wait_bar(bar(B_WF + wslot * kBoxes + b + i),
+                                                   (uint32_t)((n_w - 1) >> 1) & 1u, abort_flag, p.status,
+                                                   tmo, true))
                             ok = false;
                     if (!ok || !wait_bar(bar(B_XF + st), ph, abort_flag, p.status, tmo, true)) {
                         ok = false;
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 ptx::tc_commit(bar(B_AF + ab));
                 const bool next_fc_differs = (u + 1 >= u_end) || unit_at(p, u + 1).fc != U.fc;
-                if (next_fc_differs) ptx::tc_commit(bar(B_WE));
+                if (next_fc_differs) ptx::tc_commit(bar(B_WE + wslot));
                 if (++ab == 2) { ab = 0; aph ^= 1u; }
             }
             ptx::tc_commit(bar(B_FIN));   // all MMAs complete before TMEM is freed
@@ -263,35 +270,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------- W preparation
-        // Each chunk of W arrives raw (FP32) by TMA, one chunk ahead: thread 0
-        // fetched the first one before the block-wide sync, lane 0 of warp 2
-        // fetches each later one once the raw buffer has been converted.  Both
-        // warps convert (four columns of one W row per step) into the swizzled
-        // operand buffer, once the MMAs of the previous chunk are done with it.
-        const int tid = (warp - 2) * 32 + lane;   // 0..63
+        // Chunk m of this CTA's W goes to slot m % 2, arrives raw (FP32) by TMA
+        // and is converted in place: a 64-column box is 6 KiB both as FP32 rows
+        // and as the swizzled BF16 hi/lo operand.  Warp 2 converts the even
+        // boxes, warp 3 the odd ones, each box read whole into registers before
+        // it is overwritten.  Chunk 0 was fetched by thread 0 before the
+        // block-wide sync, chunk 1 is fetched now, chunk m + 1 (m >= 1) once the
+        // MMAs of chunk m - 1 have left its slot; so a chunk is converted while
+        // the MMAs still work on the previous one.
         const bool fetcher = warp == 2 && lane == 0;
-        int n_w = 0, prev_fc = -1, n_raw = u_begin < u_end ? 1 : 0;
+        const int wq = warp - 2;   // boxes wq, wq + 2, ...
+        int n_chunks = 0, fc_first = 0;
+        if (u_begin < u_end) {
+            fc_first = unit_at(p, u_begin).fc;
+            n_chunks = unit_at(p, u_end - 1).fc - fc_first + 1;   // units are chunk-major
+        }
+        int n_raw = n_chunks > 0 ? 1 : 0;
+        if (fetcher && n_chunks > 1) {
+            fetch_raw_w(fc_first + 1, 1);
+            n_raw = 2;
+        }
         bool ok = true;
-        for (int u = u_begin; u < u_end && ok; ++u) {
-            const Unit U = unit_at(p, u);
-            if (U.fc == prev_fc) continue;
-            prev_fc = U.fc;
-            if (!wait_bar(bar(B_WR), (uint32_t)n_w & 1u, abort_flag, p.status, tmo, true) ||
-                (n_w > 0 &&
-                 !wait_bar(bar(B_WE), (uint32_t)(n_w - 1) & 1u, abort_flag, p.status, tmo, true))) {
+        int m = 0;
+        for (; m < n_chunks && ok; ++m) {
+            const int slot = m & 1;
+            if (!wait_bar(bar(B_WR + slot), (uint32_t)(m >> 1) & 1u, abort_flag, p.status, tmo, true)) {
                 ok = false;
                 break;
             }
-            const float4* raw = reinterpret_cast<const float4*>(smem + kOffWRaw);
-            uint8_t* wsm = smem + kOffW;
-            for (int b = 0; b < kBoxes; ++b) {
-                // box b: 24 rows x 16 float4 = 384 float4, six per thread
-#pragma unroll 2
-                for (int k = 0; k < kNProj * (kBox / 4) / 64; ++k) {
-                    const int rem = tid + 64 * k;
+            uint8_t* wsm = smem + kOffW + (uint32_t)slot * kWSlot;
+            for (int b = wq; b < kBoxes; b += 2) {
+                uint8_t* box = wsm + b * kWBoxBytes;
+                // 24 rows x 16 float4 = 384 float4, twelve per lane: all read first
+                float4 v4[kNProj * (kBox / 4) / 32];
+#pragma unroll
+                for (int k = 0; k < kNProj * (kBox / 4) / 32; ++k)
+                    v4[k] = reinterpret_cast<const float4*>(box)[lane + 32 * k];
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < kNProj * (kBox / 4) / 32; ++k) {
+                    const int rem = lane + 32 * k;
                     const int j = rem >> 4, c4 = rem & 15;   // row, group of 4 columns
-                    const float4 v4 = raw[b * (kNProj * (kBox / 4)) + rem];
-                    const float v[4] = {tf32_rna(v4.x), tf32_rna(v4.y), tf32_rna(v4.z), tf32_rna(v4.w)};
+                    const float v[4] = {tf32_rna(v4[k].x), tf32_rna(v4[k].y), tf32_rna(v4[k].z),
+                                        tf32_rna(v4[k].w)};
                     uint32_t hi[2], lo[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -304,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // 128-byte swizzle: 16-byte chunk c of row n sits at chunk c ^ (n & 7);
                     // four columns are 8 bytes, half a chunk
-                    uint8_t* box = wsm + b * kWBoxBytes;
                     const int c16 = c4 >> 1, half = (c4 & 1) * 8;
                     const int nh = j, nl = kNProj + j;
                     *reinterpret_cast<uint2*>(box + nh * 128 + ((c16 ^ (nh & 7)) << 4) + half) = make_uint2(hi[0], hi[1]);
@@ -312,32 +332,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(B_WF + b));
+                if (lane == 0) ptx::mbar_arrive(bar(B_WF + slot * kBoxes + b));
             }
-            if (fetcher) FTRACE(F_W_READY, n_w);
-            ++n_w;
-            // the raw buffer is free once both warps have converted it: fetch the
-            // next chunk this CTA will need
-            int next_fc = -1;
-            for (int v = u + 1; v < u_end; ++v) {
-                const int f = unit_at(p, v).fc;
-                if (f != U.fc) { next_fc = f; break; }
-            }
-            if (fetcher && next_fc >= 0) {
-                // both warps have converted the last box, hence every box
-                if (!wait_bar(bar(B_WF + kBoxes - 1), (uint32_t)(n_w - 1) & 1u, abort_flag, p.status,
-                              tmo, true)) {
+            if (fetcher) FTRACE(F_W_READY, m);
+            // chunk m + 1 goes to slot (m + 1) % 2 once the MMAs of chunk m - 1
+            // (which also proves that chunk's conversion finished) have left it
+            if (fetcher && m >= 1 && m + 1 < n_chunks) {
+                const int ns = (m + 1) & 1;
+                if (!wait_bar(bar(B_WE + ns), (uint32_t)((m - 1) >> 1) & 1u, abort_flag, p.status, tmo,
+                              true)) {
                     ok = false;
                 } else {
-                    fetch_raw_w(next_fc);
-                    ++n_raw;
+                    fetch_raw_w(fc_first + m + 1, ns);
+                    n_raw = m + 2;
                 }
             }
             __syncwarp();
         }
         // every raw W fetch has landed before the CTA exits
-        if (fetcher && n_raw > n_w)
-            wait_bar(bar(B_WR), (uint32_t)(n_raw - 1) & 1u, abort_flag, p.status, tmo, false);
+        if (fetcher)
+            for (int c = m; c < n_raw; ++c)
+                wait_bar(bar(B_WR + (c & 1)), (uint32_t)(c >> 1) & 1u, abort_flag, p.status, tmo, false);
         __syncwarp();
     } else {
         // ---------------------------------------------------------- sum of squares, drain
