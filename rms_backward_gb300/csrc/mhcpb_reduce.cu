@@ -92,8 +92,15 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
     // Every lane of a 128-byte line (8 float4) has consumed its loads once the
     // warp has converged here; then one lane per line drops the line.
     __syncwarp();
-    if (valid && discard && (i & 7) == 0) {
-        for (int s = 0; s < S; ++s) ptx::discard_l2_line(part + (int64_t)s * n4 + i);
+    if (discard) {
+        // the warp's lines: 4 per slice (32 float4 = 512 bytes) times S slices,
+        // spread over the lanes; a line is dropped only if all of it was valid
+        const int lane = threadIdx.x & 31;
+        const int64_t w0 = i - lane;   // the warp's first float4
+        for (int q = lane; q < 4 * S; q += 32) {
+            const int64_t f4 = w0 + 8 * (q & 3);
+            if (f4 < n4) ptx::discard_l2_line(part + (int64_t)(q >> 2) * n4 + f4);
+        }
     }
 }
 

@@ -483,8 +483,10 @@ __global__ void __launch_bounds__(kReduceThreads)
     // the partials are dead once read: drop their L2 lines (a line is one
     // chunk's row for the 32 tokens of this warp)
     __syncwarp();
-    if (valid && discard && (t & 31) == 0) {
-        for (int f = 0; f < n_fc; ++f) ptx::discard_l2_line(part + (int64_t)f * stride + base);
+    if (valid && discard) {
+        // the warp's line of each chunk (32 tokens of one row), spread over the lanes
+        const int64_t b0 = base - (t & 31);
+        for (int f = t & 31; f < n_fc; f += 32) ptx::discard_l2_line(part + (int64_t)f * stride + b0);
     }
 }
 
