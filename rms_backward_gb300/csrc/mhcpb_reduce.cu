@@ -89,12 +89,12 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
         }
         dw[i] = a;
     }
-    // Every lane of a 128-byte line (8 float4) has consumed its loads once the
-    // warp has converged here; then one lane per line drops the line.
+    // Every lane of the warp has consumed its loads once the warp has converged
+    // here; then the lanes share out the discards of the lines the warp read:
+    // 4 per slice (32 float4 = 512 bytes) times S slices.  A line is dropped
+    // only if all of it was valid.
     __syncwarp();
     if (discard) {
-        // the warp's lines: 4 per slice (32 float4 = 512 bytes) times S slices,
-        // spread over the lanes; a line is dropped only if all of it was valid
         const int lane = threadIdx.x & 31;
         const int64_t w0 = i - lane;   // the warp's first float4
         for (int q = lane; q < 4 * S; q += 32) {
