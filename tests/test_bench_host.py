@@ -45,3 +45,90 @@ def test_explicit_modes():
 def test_l2_note_names_the_rule_used():
     assert "not flushed" in bench._l2_note("block", 2 * L2, None)
     assert "flushed before every timed step" in bench._l2_note("flushed", 1, None)
+
+
+# ------------------------------------------------------------------ clocks
+def _sampler_with(lines):
+    s = bench.ClockSampler(0)
+    s.lines = list(lines)
+
+    class _Done:   # stands for the finished nvidia-smi process
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s.proc = _Done()
+    return s
+
+
+def test_clock_summary_median_max_and_reasons():
+    # index, sm, max sm, power, active mask, hw, hw thermal, sw thermal, sw power cap
+    lines = [
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1100.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    out = _sampler_with(lines).stop()
+    assert out["samples"] == 3
+    assert out["sm_mhz"] == 2070.0
+    assert out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_summary_flags_thermal_and_hw_slowdown():
+    lines = ["0, 1500, 2070, 1400, 0x48, Active, Not Active, Active, Not Active"]
+    out = _sampler_with(lines).stop()
+    assert out["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    assert out["sm_mhz"] == 1500.0
+
+
+def test_clock_summary_without_nvidia_smi():
+    s = bench.ClockSampler(0)   # never started: no process
+    out = s.stop()
+    assert out["sm_mhz"] is None and out["reasons"] == ["nvidia-smi unavailable"]
+
+
+# ------------------------------------------------------------------ ncu traffic, peaks, cores
+def _fake_tree(tmp_path, traffic_hash):
+    csrc = tmp_path / "rms_backward_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in bench._STREAMING_KERNEL_SOURCES:
+        (csrc / name).write_text(f"// {name}\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    import json
+    (prof / "ncu_traffic.json").write_text(json.dumps({
+        "tcgen05": {"source_hash": traffic_hash, "dram_bytes_per_launch": 288057600}}))
+
+
+def test_ncu_traffic_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    _fake_tree(tmp_path, "0" * 16)
+    assert bench._ncu_traffic("tcgen05") is None                 # stale capture
+    current = bench._kernel_source_hash()
+    import json
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps({
+        "tcgen05": {"source_hash": current, "dram_bytes_per_launch": 288057600}}))
+    assert bench._ncu_traffic("tcgen05") == 288057600.0
+    assert bench._ncu_traffic("fma") is None                     # no capture for that kernel
+    # any change to a streaming-kernel source makes the capture stale again
+    (tmp_path / "rms_backward_gb300" / "csrc" / bench._STREAMING_KERNEL_SOURCES[0]).write_text("// edited\n")
+    assert bench._ncu_traffic("tcgen05") is None
+
+
+def test_peak_falls_back_without_measured_file(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._peaks() == (bench.FALLBACK_HBM_GBS, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6785.2}')
+    assert bench._peaks() == (6785.2, "measured")
+
+
+def test_cpu_clock_reports_cores_kept_busy():
+    c = bench._CpuClock()
+    assert c.cores() == 1.0          # nothing timed yet
+    c.wall, c.cpu = 2.0, 28.0
+    assert c.cores() == 14.0
