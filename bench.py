@@ -64,6 +64,9 @@ def _args():
                          "when the inputs are larger than L2, else flushed")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: the oracle's time budget for warm-up plus timed "
+                         "steps, which sets the tokens each step processes")
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only (for profiler runs); prints a short line")
     return ap.parse_args()
@@ -228,12 +231,12 @@ def run_reference(args):
         return 0
     import oracle.mhcpb_oracle as O
     T, K = WL.CONFIGS[WORKLOAD]["T"], WL.CONFIGS[WORKLOAD]["K"]
-    # calibrate tokens per step against a ~120 s budget for warmup + steps
+    # calibrate tokens per step against the time budget for warmup + steps
     probe = WL.make("ref_probe", T=64, K=K, seed=77)
     t0 = time.perf_counter()
     O.mhc_proj_rms_backward(probe.x, probe.w, probe.grad_proj, probe.grad_r, probe.r)
     per_token = (time.perf_counter() - t0) / 64
-    budget = 120.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     tok = int(max(1, min(T, budget / max(per_token, 1e-9))))
     wl = WL.make("ref_step", T=tok, K=K, seed=78)
     for _ in range(args.warmup):

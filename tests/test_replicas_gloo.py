@@ -5,6 +5,7 @@ combine across ranks), so N GPUs run N independent replicas; what needs to be
 right is the host logic around them: each replica draws its own inputs, every
 rank ends up with the slowest rank's time, and the whole-job value counts the
 bytes of all ranks over that time.  The reference arm runs on rank 0 only."""
+import json
 import os
 import socket
 import subprocess
@@ -70,3 +71,25 @@ def test_reference_arm_runs_on_rank_zero_only():
                          capture_output=True, text=True, env=env, timeout=120)
     assert out.returncode == 0
     assert out.stdout.strip() == ""
+
+
+def test_reference_arm_line_on_rank_zero():
+    """The reference arm (the oracle on the host cores) prints one JSON line
+    with the bench's keys; a short time budget keeps this a CPU test."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "1", "--ref-seconds", "3"],
+                         capture_output=True, text=True, env=env, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1
+    for key in ("metric", "value", "unit", "ms_per_step", "higher_is_better", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["sample_tokens_per_step"] >= 1
