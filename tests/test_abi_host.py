@@ -3,6 +3,7 @@ function ``include/mhcpb.h`` declares, and rejects bad flags and shapes before
 making any CUDA call (the cuDNN frontend page "DSv4.1 mHC projection/RMS
 backward", "Requirements and tensor contract": other shapes and precisions are
 rejected; allow_tf32 must be passed explicitly)."""
+import ctypes
 import os
 import re
 
@@ -104,3 +105,49 @@ def test_missing_library_fails_loudly():
             "    print('raised', 'missing' in str(e))\n" % ROOT)
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
     assert out.stdout.strip() == "raised True", out.stdout + out.stderr
+
+
+_SCALARS = {"int64_t": ctypes.c_int64, "uint64_t": ctypes.c_uint64, "int": ctypes.c_int,
+            "uint32_t": ctypes.c_uint32, "size_t": ctypes.c_size_t, "float": ctypes.c_float,
+            "mhcpb_status_t": ctypes.c_int}
+_POINTERS = ("mhcpb_plan_t",)   # typedef of a struct pointer
+
+
+def declared_signatures():
+    """(return type, [parameter types]) of every function the header declares."""
+    text = re.sub(r"/\*.*?\*/", " ", open(HEADER).read(), flags=re.S)
+    out = {}
+    for ret, name, params in re.findall(
+            r"(mhcpb_status_t|const\s+char\s*\*)\s*(mhcpb_[a-z_]+)\s*\(([^)]*)\)\s*;", text):
+        types = []
+        for p in (q.strip() for q in params.split(",")):
+            if p in ("", "void"):
+                continue
+            types.append(re.sub(r"\s*\b[A-Za-z_][A-Za-z0-9_]*$", "", p).strip())   # drop the name
+        out[name] = (ret.replace(" ", ""), types)
+    return out
+
+
+def _same_kind(c_type, ct):
+    if "*" in c_type or c_type in _POINTERS:
+        return ct is ctypes.c_void_p or issubclass(ct, ctypes._Pointer)
+    base = _SCALARS[c_type.replace("const ", "")]
+    return ctypes.sizeof(ct) == ctypes.sizeof(base) and (ct is base or ct._type_ == base._type_)
+
+
+def test_binding_signatures_match_the_header(lib):
+    """The ctypes declarations agree with the C prototypes: the same number of
+    arguments and, position by position, the same size and pointer-ness (a
+    mismatch would pass garbage through the ABI without any error)."""
+    sigs = declared_signatures()
+    assert set(sigs) == set(declared_functions())
+    for name, (ret, types) in sigs.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == len(types), (name, types, fn.argtypes)
+        for i, (c_type, ct) in enumerate(zip(types, fn.argtypes)):
+            assert _same_kind(c_type, ct), (name, i, c_type, ct)
+        if ret == "mhcpb_status_t":
+            assert fn.restype in (ctypes.c_int, ctypes.c_int32), name
+        else:
+            assert fn.restype is ctypes.c_char_p, name
