@@ -151,3 +151,35 @@ def test_binding_signatures_match_the_header(lib):
             assert fn.restype in (ctypes.c_int, ctypes.c_int32), name
         else:
             assert fn.restype is ctypes.c_char_p, name
+
+
+def _header_constants():
+    text = re.sub(r"/\*.*?\*/", " ", open(HEADER).read(), flags=re.S)
+    consts = {}
+    for name, expr in re.findall(r"\b(MHCPB_[A-Z0-9_]+)\s*=\s*([^,}\n]+)", text):
+        consts[name] = expr
+    for name, expr in re.findall(r"#define\s+(MHCPB_[A-Z0-9_]+)\s+(\([^)\n]*\)|[0-9][^\s]*)", text):
+        consts[name] = expr
+    out = {}
+    for name, expr in consts.items():
+        py = re.sub(r"(\d)u\b", r"\1", expr.strip())
+        if re.fullmatch(r"[0-9()<\s+*-]+", py):
+            out[name] = eval(py)   # integer literals and shifts only (checked above)
+    return out
+
+
+def test_binding_constants_match_the_header():
+    consts = _header_constants()
+    for name in ("MHCPB_OK", "MHCPB_ERR_SCRATCH_TOO_SMALL", "MHCPB_ALLOW_TF32",
+                 "MHCPB_TEST_INJECT_STALL", "MHCPB_STATIC_SCRATCH_BYTES", "MHCPB_NPROJ"):
+        assert name in consts, name           # the parser sees both forms
+    checked = 0
+    for name, value in consts.items():
+        if hasattr(abi, name) and not callable(getattr(abi, name)):
+            assert getattr(abi, name) == value, name
+            checked += 1
+    assert checked >= 20
+    # the macro of the partial size: 512 tokens for every T
+    m = re.search(r"#define\s+MHCPB_PARTIAL_TOKENS\(T\)\s+(\d+)", open(HEADER).read())
+    for T in (1, 512, 4096, 1 << 24):
+        assert abi.MHCPB_PARTIAL_TOKENS(T) == int(m.group(1))
