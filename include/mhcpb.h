@@ -168,7 +168,12 @@ mhcpb_status_t mhcpb_execute(mhcpb_plan_t plan,
  *   dX is final and `workspace` holds the dW partials of these inputs.
  *   mhcpb_reduce_dw:  enqueues the reduction only: dW from the partials that
  *   the last mhcpb_execute_dx with this workspace left there (overwritten, or
- *   accumulated with MHCPB_ACCUMULATE_DW).
+ *   accumulated with MHCPB_ACCUMULATE_DW).  It only reads the workspace, so
+ *   it may be repeated on the same partials (e.g. a retried step, or the same
+ *   partials accumulated into two dW buffers); each call gives the same sum.
+ *   (mhcpb_execute, which writes and reduces the partials in one call, may
+ *   drop them from L2 once summed: after it the workspace holds nothing
+ *   reusable.)
  *
  * Arguments, checks and status codes are those of mhcpb_execute for the
  * operands each call uses.  The caller orders the two (same stream, or an
@@ -249,12 +254,16 @@ mhcpb_status_t mhcpb_plan_set_max_ctas(mhcpb_plan_t plan, int max_ctas);
  *  - The first call on a device does that device's set-up (looks up the
  *    buffer's device address, raises the kernels' shared-memory limit).  Make
  *    that first call before any stream capture.
- *  - Every call, on every stream, shares the one buffer and leaves the last
- *    call's partials in it (nothing in it needs to start at zero: each execute
- *    overwrites every partial it reads).  Calls that may overlap on the GPU
- *    race on the buffer: order them on one stream or with events.
- *  - A device-side wait timeout leaves the outputs undefined and is recorded
- *    in a device word that this entry point does not report. */
+ *  - Every call, on every stream, shares the one buffer.  Nothing in it needs
+ *    to start at zero (each call overwrites every partial it reads) and
+ *    nothing in it is meant to be read afterwards (the reduction may drop the
+ *    partials from L2 once summed).  Calls that may overlap on the GPU race on
+ *    the buffer: order them on one stream or with events.
+ *  - Every wait inside the kernels is bounded by a fixed 1 s (there is no plan
+ *    to set another limit on).  A wait that runs out leaves the outputs
+ *    undefined and is recorded in a device word that the kernels only ever
+ *    write: this entry point neither reports nor clears it, so a timeout is
+ *    not visible to the caller beyond the wrong outputs. */
 mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uint32_t flags,
                                             const void* x, const float* w, const float* grad_proj,
                                             const float* grad_r, const float* r,

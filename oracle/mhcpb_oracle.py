@@ -286,7 +286,10 @@ def check_dx_addend(dx_bits, ref_bits, core_ref_bits, core_abs_bound, ulps=2.0,
     u = bf16_ulp(b)
     lim = np.maximum(ulps * u, ulps * bf16_ulp(core) + rel_abs * np.asarray(core_abs_bound) + u)
     ok_elem = np.where(fin, (diff <= lim) & np.isfinite(a), (np.isnan(a) & np.isnan(b)) | (a == b))
+    within_ulps = diff <= ulps * u
     stats = dict(n=int(a.size), fail=int((~ok_elem).sum()),
+                 ulp_pass=int((within_ulps & fin).sum()),
+                 abs_only_pass=int((~within_ulps & (diff <= lim) & fin).sum()),
                  exact=int((np.asarray(dx_bits) == np.asarray(ref_bits)).sum()),
                  max_ulp=float(np.max(np.where(fin, diff / u, 0.0))) if a.size else 0.0)
     return bool(ok_elem.all()), stats

@@ -396,9 +396,11 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, int what, const void* x, c
     if (ev1 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev1), st)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord");
     if (run2) {
+        // partials written by this same call are dead after the sum (their L2
+        // lines may be dropped); a stand-alone reduction leaves them intact
         e = launch_reduce(static_cast<const float*>(workspace), dw, plan->S, (int64_t)kNProj * K,
                           (plan->flags & MHCPB_COMPENSATED_DW) != 0,
-                          (plan->flags & MHCPB_ACCUMULATE_DW) != 0, st);
+                          (plan->flags & MHCPB_ACCUMULATE_DW) != 0, run1, st);
         if (e != cudaSuccess) return cuda_fail(e, "launch (dW reduction)");
     }
     if (ev2 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev2), st)) != cudaSuccess)

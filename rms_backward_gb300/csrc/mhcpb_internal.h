@@ -134,7 +134,9 @@ int record_cuda_error(cudaError_t e, const char* what);
 // Second kernel: dW[j,k] = sum over s ascending of partial[s][j][k]; with
 // `compensated`, TwoSum at every addition and one final rounding; with
 // `accumulate`, the result is added to dW's previous contents.
+// `discard`: drop the partials' L2 lines after reading them (their contents
+// are then undefined), only where nothing reads them again.
 cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, bool compensated,
-                          bool accumulate, cudaStream_t stream);
+                          bool accumulate, bool discard, cudaStream_t stream);
 
 }  // namespace mhcpb

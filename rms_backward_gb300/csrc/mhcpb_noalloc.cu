@@ -152,7 +152,7 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
         return (mhcpb_status_t)record_cuda_error(e, "launch (tensor-core kernel)");
     if ((e = launch_reduce(p.partial, dw, p.S, (int64_t)kNProj * K,
                            (flags & MHCPB_COMPENSATED_DW) != 0,
-                           (flags & MHCPB_ACCUMULATE_DW) != 0, st)) != cudaSuccess)
+                           (flags & MHCPB_ACCUMULATE_DW) != 0, true, st)) != cudaSuccess)
         return (mhcpb_status_t)record_cuda_error(e, "launch (dW reduction)");
     return MHCPB_OK;
 }

@@ -21,9 +21,11 @@
 // cake_rmsnorm_det_train_backward describes the same idea for its small-T dw
 // column sums.  Launched as a
 // programmatic dependent of the streaming kernel: it may be scheduled while
-// that kernel drains and waits for its completion before reading.  The
-// partials are dead once read: with a 128-byte-aligned workspace their L2
-// lines are dropped without being written back to HBM.
+// that kernel drains and waits for its completion before reading.  When the
+// same call wrote the partials (nothing reads them again), they are dead once
+// read: with a 128-byte-aligned workspace their L2 lines are dropped without
+// being written back to HBM.  A stand-alone reduction (the split call) keeps
+// them, so it can be repeated on the same workspace.
 #include "mhcpb_internal.h"
 #include "ptx.cuh"
 
@@ -107,11 +109,12 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
 }  // namespace
 
 cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, bool compensated,
-                          bool accumulate, cudaStream_t stream) {
+                          bool accumulate, bool discard_allowed, cudaStream_t stream) {
     const int64_t n4 = n / 4;
     // discard needs 128-byte-aligned lines: every s-slice starts at a multiple
     // of 96 K bytes (K % 8 == 0, so a multiple of 768) from the base
-    const int discard = (reinterpret_cast<uintptr_t>(partial) & 127u) == 0 ? 1 : 0;
+    const int discard =
+        discard_allowed && (reinterpret_cast<uintptr_t>(partial) & 127u) == 0 ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((n4 + kReduceThreads - 1) / kReduceThreads));
     cfg.blockDim = dim3(kReduceThreads);

@@ -76,6 +76,33 @@ def assert_parity_full(wl, dx, dw, label=""):
     return st, stw
 
 
+def assert_parity_all_rows(wl, dx, dw, label="", block=256):
+    """Every element of dX and dW against the oracle at any size: the oracle
+    computes dX one block of rows at a time (its own row selection) so its
+    FP64 arrays stay small, and dW over all columns.  Returns the merged
+    check statistics."""
+    T = wl.T
+    tot = dict(n=0, fail=0, exact=0, max_ulp=0.0, abs_only_pass=0)
+    for r0 in range(0, T, block):
+        rows = np.arange(r0, min(T, r0 + block))
+        ref_dx, _ = O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r,
+                                            addend_bits=wl.addend, rows=rows)
+        bound = O.dx_abs_bound(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r, rows=rows)
+        if wl.addend is not None:
+            core, _ = O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r, rows=rows)
+            ok, st = O.check_dx_addend(dx[rows], ref_dx, core, bound)
+        else:
+            ok, st = O.check_dx(dx[rows], ref_dx, bound)
+        assert ok, f"{label} dX mismatch in rows {r0}..{rows[-1]}: {st}"
+        for k in ("n", "fail", "exact", "abs_only_pass"):
+            tot[k] += st.get(k, 0)
+        tot["max_ulp"] = max(tot["max_ulp"], st["max_ulp"])
+    ref_dw = O.dw_f64(wl.x, wl.grad_proj)
+    okw, stw = O.check_dw(dw, ref_dw, O.dw_abs_bound(wl.x, wl.grad_proj))
+    assert okw, f"{label} dW mismatch: {stw}"
+    return tot, stw
+
+
 def sample_rows(T, n=48, seed=0):
     rng = np.random.default_rng(seed)
     fixed = [0, 1, 127, 128, 511, 512, T - 1, T - 2, T // 2]

@@ -54,6 +54,43 @@ def test_split_equals_fused(fma, addend):
     torch.cuda.synchronize()
     assert plan.device_status() == 0
     assert torch.equal(dw.view(torch.int32), ref_dw.view(torch.int32))
+    # and against the oracle, every element of both outputs
+    st = assert_parity_full(wl, dx.view(torch.int16).cpu().numpy().view(np.uint16), dw.cpu().numpy(),
+                            "split")
+    print(f"split fma={fma} addend={addend}: dX {st[0]} dW {st[1]}")
+    plan.close()
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_reduce_dw_twice_on_one_workspace(accumulate):
+    """mhcpb_reduce_dw only reads the partials: a second call on the same
+    workspace sums the same values again (the same bits, or with
+    MHCPB_ACCUMULATE_DW the same D added a second time)."""
+    wl = WL.make("twice", T=1600, K=776, seed=65)
+    i = to_dev(wl)
+    _, d = _fused(wl, i)
+    dn = d.cpu().numpy()
+    plan = Plan(wl.T, wl.K, 0, accumulate_dw=accumulate)
+    dx, dw, ws = _bufs(wl, plan)
+    plan.execute_dx(i["x"], i["w"], i["grad_proj"], i["grad_r"], i["r"], dx, ws)
+    rng = np.random.default_rng(8)
+    dw_in = (rng.standard_normal((24, wl.K)) * 2).astype(np.float32)
+    if accumulate:
+        dw.copy_(torch.from_numpy(dw_in))
+    plan.reduce_dw(ws, dw)
+    torch.cuda.synchronize()
+    first = dw.cpu().numpy().copy()
+    plan.reduce_dw(ws, dw)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    second = dw.cpu().numpy()
+    if accumulate:
+        want1 = (dw_in + dn).astype(np.float32)
+        assert np.array_equal(first.view(np.uint32), want1.view(np.uint32))
+        assert np.array_equal(second.view(np.uint32), (want1 + dn).astype(np.float32).view(np.uint32))
+    else:
+        assert np.array_equal(first.view(np.uint32), dn.view(np.uint32))
+        assert np.array_equal(second.view(np.uint32), dn.view(np.uint32))
     plan.close()
 
 
