@@ -1,9 +1,10 @@
 """Host logic of bench.py that decides how steps are timed (no GPU needed).
 
 Timing rule: between timed steps either flush L2 or use inputs larger than
-L2.  Block timing (K steps back to back between one pair of events, no flush)
-is chosen only when the step's inputs exceed L2; otherwise every step is
-preceded by a flush."""
+L2.  The headline flushes L2 before every step and takes the median of the
+per-step times; block timing (K steps back to back between one pair of
+events, no flush) is a side figure, allowed only when the step's inputs
+exceed L2."""
 import os
 import sys
 from types import SimpleNamespace
@@ -27,12 +28,25 @@ def _mode(timing, input_bytes):
     return bench._timing_mode(SimpleNamespace(timing=timing), input_bytes, None)
 
 
-def test_auto_picks_block_only_for_inputs_larger_than_l2():
+def test_headline_default_is_flushed():
     x_training_profile = 2 * 4096 * 20480          # 168 MB of BF16 X
-    x_edge = 2 * 1000 * 20480                      # 41 MB
-    assert _mode("auto", x_training_profile) == "block"
-    assert _mode("auto", x_edge) == "flushed"
-    assert _mode("auto", L2) == "flushed"          # not larger: flush
+    import sys as _s
+    argv, _s.argv = _s.argv, ["bench.py"]
+    try:
+        args = bench._args()
+    finally:
+        _s.argv = argv
+    assert args.timing == "flushed"
+    assert _mode(args.timing, x_training_profile) == "flushed"
+    assert args.steps >= 50                        # the median is over >= 50 flushed steps
+
+
+def test_flushed_median_and_stats():
+    import numpy as np
+    times = [1.0, 3.0, 2.0, 100.0, 2.5]            # ms; one outlier
+    st = bench._stats_us(times)
+    assert st["reps"] == 5 and st["median_us"] == 2500.0
+    assert st["min_us"] == 1000.0 and st["mean_us"] == np.mean(times) * 1e3
 
 
 def test_explicit_modes():

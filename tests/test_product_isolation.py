@@ -64,7 +64,8 @@ def test_oracle_imports_nothing_of_the_cuda_path():
 def test_entry_points_import_the_oracle_only_where_allowed():
     allowed = {
         "__graft_entry__.py": {"smoke"},
-        "bench.py": {"_oracle_rate", "run_reference", "run_forward"},
+        # _cpu_worker: the child process the CPU-baseline leg starts
+        "bench.py": {"_cpu_worker", "run_reference", "run_forward"},
     }
     for name, funcs in allowed.items():
         found = _oracle_imports(os.path.join(ROOT, name))
@@ -77,6 +78,10 @@ def test_entry_points_import_the_oracle_only_where_allowed():
         if func == "run_forward":
             above = "\n".join(src[max(0, line - 4):line - 1])
             assert "no_cpu_baseline" in above, line
+    # the CPU worker runs only from the CPU-baseline leg: main() starts it for
+    # --cpu-worker, which only _cpu_baseline_protocol passes
+    text = "\n".join(src)
+    assert text.count('"--cpu-worker"') == 2   # the option and the one call that sets it
 
 
 def test_importing_the_library_loads_no_oracle():
