@@ -123,6 +123,38 @@ def make(name: str, T: int, K: int, seed: int, *, addend: bool = False,
     )
 
 
+@dataclass
+class GateWorkload:
+    """Inputs of the gate/normalisation step (draws only; see make_gates)."""
+    name: str
+    T: int
+    seed: int
+    proj: np.ndarray     # float32 [T, 32]: projection logits (columns 24..31 unused)
+    r: np.ndarray        # float32 [T]: RMS of each row
+    alpha: np.ndarray    # float32 [3]: scales of the pre, post and res logits
+    bias: np.ndarray     # float32 [24]
+    grad_h: np.ndarray   # float32 [T, 24]: upstream gradients of H_pre, H_post, H_res
+
+
+def make_gates(name: str, T: int, seed: int) -> GateWorkload:
+    """Draw the gate step's inputs at the training profile's scale: proj has
+    the spread of X W^T for X ~ N(0, 1) and W ~ N(0, 0.02) over K = 20480
+    (standard deviation 0.02 sqrt(20480) = 2.86), r the RMS of such rows
+    (about 1, here U(0.9, 1.1)), alpha = 0.5 U(0.5, 1.5) each, bias ~ N(0, 0.5),
+    grad_h ~ N(0, 1e-2); proj[:, 24:32] = +-1e30 (never read).  Draw order:
+    proj, r, alpha, bias, grad_h, signs of the unused columns."""
+    g = torch.Generator().manual_seed(seed)
+    proj = torch.randn(T, GRAD_PROJ_COLS, generator=g, dtype=torch.float32) * 2.862
+    r = 0.9 + 0.2 * torch.rand(T, generator=g, dtype=torch.float32)
+    alpha = 0.5 * (0.5 + torch.rand(3, generator=g, dtype=torch.float32))
+    bias = torch.randn(N_PROJ, generator=g, dtype=torch.float32) * 0.5
+    gh = torch.randn(T, N_PROJ, generator=g, dtype=torch.float32) * 1e-2
+    sign = torch.where(torch.rand(T, 8, generator=g) < 0.5, -1.0, 1.0)
+    proj[:, N_PROJ:] = 1e30 * sign
+    return GateWorkload(name=name, T=T, seed=seed, proj=proj.numpy(), r=r.numpy(),
+                        alpha=alpha.numpy(), bias=bias.numpy(), grad_h=gh.numpy())
+
+
 def make_dw_cancellation(K: int, seed: int, chunk: int = 512) -> Workload:
     """Three chunks of ``chunk`` tokens whose dW contributions are 2**24, 1 and
     1 for every (j, k): X is zero except X[0, :] = 2**24, X[chunk, :] = 1 and
