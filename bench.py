@@ -405,6 +405,34 @@ def _forward_side(plan, x, w, flush, stream, T, K, peak, reps=100):
             "kernel_algorithmic_bytes": k1_bytes}
 
 
+def _gates_side(T, flush, stream, peak, reps=100, n_iter=20):
+    """The gate/normalisation step at T tokens (its own seeded inputs): the
+    backward (grad_proj and grad_r from the gates' gradients) and the forward,
+    flushed per-call medians."""
+    import torch
+    from rms_backward_gb300 import mhc_gate_backward, mhc_gate_forward
+    g = WL.make_gates("bench_gates", T=T, seed=11)
+    dev = flush.device
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    proj, r, al, b, gh = f(g.proj), f(g.r), f(g.alpha), f(g.bias), f(g.grad_h)
+    gp = torch.empty((T, 32), dtype=torch.float32, device=dev)
+    gr = torch.empty((T,), dtype=torch.float32, device=dev)
+    h = torch.empty((T, 24), dtype=torch.float32, device=dev)
+    out = {}
+    for name, call, nbytes in (
+            ("backward", lambda: mhc_gate_backward(proj, r, al, b, gh, gp, gr, n_iter=n_iter, stream=stream),
+             T * (96 + 4 + 96 + 128 + 4)),
+            ("forward", lambda: mhc_gate_forward(proj, r, al, b, h, n_iter=n_iter, stream=stream),
+             T * (96 + 4 + 96))):
+        for _ in range(5):
+            call()
+        st = _stats_us(_step_times(call, flush, reps, "flushed", stream))
+        gbs = nbytes / (st["median_us"] * 1e-6) / 1e9
+        out[name] = dict(st, algorithmic_bytes=nbytes, achieved_gbs=gbs, frac_of_hbm_peak=gbs / peak)
+    out["config"] = {"T": T, "n_iter": n_iter, "threads_per_token": 16}
+    return out
+
+
 def _cpu_worker(spec):
     """Child process of the CPU baseline: times the oracle on one config with
     the cores the parent left it; prints one JSON line."""
@@ -638,8 +666,10 @@ def run_ours(args):
     e2e_value = _aggregate_gbs(alg, world, e2e_ms)
 
     fwd = None
+    gates = None
     if not args.no_forward and not has_add:
         fwd = _forward_side(plan, x, w, flush, stream, T, K, peak)
+        gates = _gates_side(T, flush, stream, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
@@ -681,6 +711,7 @@ def run_ours(args):
                          "reduce_us": k2_ms * 1e3,
                          "algorithmic_bytes_per_launch": k1_bytes},
             "forward": fwd,
+            "gates": gates,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": 2 * args.steps,

@@ -306,6 +306,47 @@ mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const fl
                                       size_t workspace_bytes, void* stream, void* ev_before,
                                       void* ev_between, void* ev_after);
 
+/* ---------------------------------------------------------------------------
+ * The gate/normalisation step around the stage: the forward turns the
+ * projection logits and r into the mHC gates; the backward turns the gates'
+ * upstream gradients into this stage's inputs grad_proj and grad_r.  The
+ * cuDNN page (intro) places "the gate and normalization derivatives" before
+ * the stage and leaves "Sinkhorn, gate derivatives" to the caller; the
+ * prime-kernels PR #15 page ("mhc_projection") fuses "gate activations
+ * (sigmoid, Sinkhorn)" into the projection.  Neither page writes the
+ * formulas; these calls compute this reading of them (n = 4 streams, so the
+ * 24 projection columns are 2n + n^2 logits):
+ *
+ *     columns 0..3 pre, 4..7 post, 8..23 res (row-major 4 x 4: 8 + 4i + j)
+ *     l[t, j]  = a_g(j) * proj[t, j] / r[t] + b[j]       a = (a_pre, a_post, a_res)
+ *     H_pre    = sigmoid(l_pre)
+ *     H_post   = 2 sigmoid(l_post)
+ *     H_res    = Sinkhorn(exp(l_res)): n_iter times, every row divided by its
+ *                sum, then every column divided by its sum
+ *
+ * and the backward, for upstream gradients G in H's layout, the exact chain
+ * rule: dl = dL/dl, grad_proj[t, j] = dl[t, j] a_g(j) / r[t] (columns 24..31
+ * written as zero), grad_r[t] = -sum_j dl[t, j] a_g(j) proj[t, j] / r[t]^2.
+ * The parameter gradients of a and b stay with the caller (the cuDNN page
+ * leaves parameter-gradient accumulation to it); `dlogits`, if not NULL,
+ * receives dl [T, 24] for that.
+ *
+ * Layouts (all FP32, row-major): proj [T, 32] (columns 24..31 not read), r [T],
+ * alpha [3], bias [24], h and grad_h [T, 24], grad_proj [T, 32], grad_r [T].
+ * FP32 arithmetic; results within 1e-4 of each token's largest magnitude of
+ * the exact values.  1 <= T <= MHCPB_MAX_T, 1 <= n_iter <= MHCPB_GATE_MAX_ITER
+ * (else MHCPB_ERR_UNSUPPORTED_SHAPE).  No plan and no workspace: the calls
+ * run on the calling thread's current device, where every pointer must be
+ * device memory (MHCPB_ERR_WRONG_DEVICE), 4-byte aligned (MHCPB_ERR_MISALIGNED);
+ * outputs may not overlap each other or any input (MHCPB_ERR_ALIASING).
+ * Enqueued on `stream`; nothing is allocated; outputs are overwritten. */
+#define MHCPB_GATE_MAX_ITER 64
+mhcpb_status_t mhcpb_gate_forward(int64_t T, int n_iter, const float* proj, const float* r,
+                                  const float* alpha, const float* bias, float* h, void* stream);
+mhcpb_status_t mhcpb_gate_backward(int64_t T, int n_iter, const float* proj, const float* r,
+                                   const float* alpha, const float* bias, const float* grad_h,
+                                   float* grad_proj, float* grad_r, float* dlogits, void* stream);
+
 /* Releases the plan (and its status word).  Safe on NULL. */
 mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan);
 

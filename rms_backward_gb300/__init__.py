@@ -136,3 +136,29 @@ def mhc_projection_backward(x, weight, grad_proj, grad_r, r, addend=None, *, str
         torch.cuda.synchronize(x.device)
     plan.close()
     return dx, dw
+
+
+def _stream_handle(stream, like):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream(like.device).cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def mhc_gate_forward(proj, r, alpha, bias, h, *, n_iter: int = 20, stream=None):
+    """Gates H [T, 24] (H_pre, H_post, H_res row-major) from the projection
+    logits proj [T, 32] and r [T] (FP32 CUDA tensors); writes h."""
+    from . import abi
+    abi.mhcpb_gate_forward(proj.shape[0], n_iter, proj.data_ptr(), r.data_ptr(), alpha.data_ptr(),
+                           bias.data_ptr(), h.data_ptr(), _stream_handle(stream, proj))
+
+
+def mhc_gate_backward(proj, r, alpha, bias, grad_h, grad_proj, grad_r, dlogits=None, *,
+                      n_iter: int = 20, stream=None):
+    """grad_proj [T, 32] and grad_r [T] (the projection/RMS backward's inputs)
+    from the gates' upstream gradients grad_h [T, 24]; dlogits [T, 24] if given."""
+    from . import abi
+    abi.mhcpb_gate_backward(proj.shape[0], n_iter, proj.data_ptr(), r.data_ptr(), alpha.data_ptr(),
+                            bias.data_ptr(), grad_h.data_ptr(), grad_proj.data_ptr(),
+                            grad_r.data_ptr(), None if dlogits is None else dlogits.data_ptr(),
+                            _stream_handle(stream, proj))

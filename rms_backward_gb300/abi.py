@@ -40,6 +40,7 @@ def MHCPB_PARTIAL_TOKENS(T: int) -> int:
     return 512
 
 MHCPB_STATIC_SCRATCH_BYTES = 16 << 20
+MHCPB_GATE_MAX_ITER = 64
 
 QUERY = {"T": 0, "K": 1, "S": 2, "grid": 3, "flags": 4, "smem": 5, "token_tile": 6, "strip": 7,
          "partial_tokens": 8}
@@ -49,7 +50,7 @@ EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcp
             "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error",
             "mhcpb_execute_static_scratch", "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx",
             "mhcpb_reduce_dw", "mhcpb_forward_workspace_bytes", "mhcpb_forward",
-            "mhcpb_forward_profiled")
+            "mhcpb_forward_profiled", "mhcpb_gate_forward", "mhcpb_gate_backward")
 
 
 class MhcpbError(RuntimeError):
@@ -89,6 +90,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_forward_workspace_bytes.argtypes = [P, ctypes.POINTER(SZ)]
     lib.mhcpb_forward.argtypes = [P, P, P, ctypes.c_float, P, P, P, SZ, P]
     lib.mhcpb_forward_profiled.argtypes = [P, P, P, ctypes.c_float, P, P, P, SZ, P, P, P, P]
+    lib.mhcpb_gate_forward.argtypes = [I64, I32, P, P, P, P, P, P]
+    lib.mhcpb_gate_backward.argtypes = [I64, I32, P, P, P, P, P, P, P, P, P]
     lib.mhcpb_destroy.argtypes = [P]
     lib.mhcpb_status_string.argtypes = [I32]
     lib.mhcpb_status_string.restype = ctypes.c_char_p
@@ -98,7 +101,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "mhcpb_execute_profiled", "mhcpb_get_device_status", "mhcpb_plan_query",
                  "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch",
                  "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx", "mhcpb_reduce_dw",
-                 "mhcpb_forward_workspace_bytes", "mhcpb_forward", "mhcpb_forward_profiled"):
+                 "mhcpb_forward_workspace_bytes", "mhcpb_forward", "mhcpb_forward_profiled",
+                 "mhcpb_gate_forward", "mhcpb_gate_backward"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -203,3 +207,20 @@ def mhcpb_execute_static_scratch(T: int, K: int, flags: int, x: int, w: int, gra
     _check(load().mhcpb_execute_static_scratch(int(T), int(K), int(flags), x, w, grad_proj, grad_r,
                                                r, dx, dw, grad_x_addend or None, stream or None),
            "mhcpb_execute_static_scratch")
+
+
+def mhcpb_gate_forward(T: int, n_iter: int, proj: int, r: int, alpha: int, bias: int, h: int,
+                       stream: int | None) -> None:
+    """Gates from the projection logits and r: H_pre, H_post, H_res [T, 24]."""
+    _check(load().mhcpb_gate_forward(int(T), int(n_iter), proj, r, alpha, bias, h, stream or None),
+           "mhcpb_gate_forward")
+
+
+def mhcpb_gate_backward(T: int, n_iter: int, proj: int, r: int, alpha: int, bias: int,
+                        grad_h: int, grad_proj: int, grad_r: int, dlogits: int | None,
+                        stream: int | None) -> None:
+    """grad_proj [T, 32] and grad_r [T] (and optionally dL/dlogits [T, 24])
+    from the gates' upstream gradients."""
+    _check(load().mhcpb_gate_backward(int(T), int(n_iter), proj, r, alpha, bias, grad_h, grad_proj,
+                                      grad_r, dlogits or None, stream or None),
+           "mhcpb_gate_backward")

@@ -1,0 +1,181 @@
+// Gate/normalisation step of mHC around the projection/RMS stage, forward and
+// backward (the backward produces the stage's grad_proj and grad_r).
+//
+// The cuDNN frontend page "DSv4.1 mHC projection/RMS backward" (intro) feeds
+// the stage "the upstream projection and RMS gradients after the gate and
+// normalization derivatives"; the prime-kernels PR #15 page ("mhc_projection")
+// fuses "gate activations (sigmoid, Sinkhorn)" into the projection.  Neither
+// prints the formulas; this file computes the reading stated in mhcpb.h
+// (mhcpb_gate_forward): for n = 4 streams the 24 projection columns are the
+// 4 pre, 4 post and 16 residual logits
+//     l = a_g * proj / r + b,  H_pre = sigmoid(l), H_post = 2 sigmoid(l),
+//     H_res = Sinkhorn(exp(l)) (row normalisation then column normalisation,
+//     n_iter times)
+// and the backward is its exact chain rule.
+//
+// GB300 layout: a half-warp per token, lane i*4+j owns residual entry (i, j)
+// (and lane g < 8 also pre/post gate g), so every row sum is a 2-step and every
+// column sum a 2-step shuffle inside the half-warp.  FP32 throughout.  The
+// exponentials are taken after subtracting each row's maximum: the first row
+// normalisation makes the result (and its gradient) independent of any
+// per-row factor, so this changes nothing but the range.  The backward keeps
+// the matrix before each row normalisation in shared memory (one float per
+// lane and iteration) and recomputes the rest on the way back.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mhcpb.h"
+#include "mhcpb_internal.h"
+
+namespace mhcpb {
+namespace gates {
+
+namespace {
+
+constexpr int kThreads = 256;            // 16 tokens per block
+constexpr int kTokensPerBlock = kThreads / 16;
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float row_sum(float v) {   // lanes 4i .. 4i+3 of the half-warp
+    v += __shfl_xor_sync(kFull, v, 1, 16);
+    v += __shfl_xor_sync(kFull, v, 2, 16);
+    return v;
+}
+__device__ __forceinline__ float col_sum(float v) {   // lanes j, j+4, j+8, j+12
+    v += __shfl_xor_sync(kFull, v, 4, 16);
+    v += __shfl_xor_sync(kFull, v, 8, 16);
+    return v;
+}
+__device__ __forceinline__ float row_max(float v) {
+    v = fmaxf(v, __shfl_xor_sync(kFull, v, 1, 16));
+    v = fmaxf(v, __shfl_xor_sync(kFull, v, 2, 16));
+    return v;
+}
+__device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
+
+struct Lane {
+    int64_t t;       // token
+    int l;           // lane within the half-warp: residual entry (l / 4, l % 4)
+    bool valid;      // t < T (invalid lanes still take part in the shuffles)
+};
+__device__ __forceinline__ Lane lane_of(int64_t T) {
+    Lane L;
+    L.t = (int64_t)blockIdx.x * kTokensPerBlock + (threadIdx.x >> 4);
+    L.l = threadIdx.x & 15;
+    L.valid = L.t < T;
+    return L;
+}
+
+// exp of this lane's residual logit after subtracting its row's maximum
+__device__ __forceinline__ float res_exp(float lres) { return expf(lres - row_max(lres)); }
+
+__global__ void __launch_bounds__(kThreads) gate_forward_kernel(int64_t T, int n_iter,
+                                                                 const float* __restrict__ proj,
+                                                                 const float* __restrict__ r,
+                                                                 const float* __restrict__ alpha,
+                                                                 const float* __restrict__ bias,
+                                                                 float* __restrict__ h) {
+    const Lane L = lane_of(T);
+    const float rv = L.valid ? r[L.t] : 1.f;
+    const float pres = L.valid ? proj[L.t * 32 + 8 + L.l] : 0.f;
+    float A = res_exp(alpha[2] * pres / rv + bias[8 + L.l]);
+    for (int k = 0; k < n_iter; ++k) {
+        const float R = A / row_sum(A);
+        A = R / col_sum(R);
+    }
+    if (!L.valid) return;
+    h[L.t * kNProj + 8 + L.l] = A;
+    if (L.l < 8) {
+        const float a = L.l < 4 ? alpha[0] : alpha[1];
+        const float s = sigmoid(a * proj[L.t * 32 + L.l] / rv + bias[L.l]);
+        h[L.t * kNProj + L.l] = L.l < 4 ? s : 2.f * s;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) gate_backward_kernel(
+    int64_t T, int n_iter, const float* __restrict__ proj, const float* __restrict__ r,
+    const float* __restrict__ alpha, const float* __restrict__ bias,
+    const float* __restrict__ grad_h, float* __restrict__ grad_proj, float* __restrict__ grad_r,
+    float* __restrict__ dlogits) {
+    extern __shared__ float iters[];   // [n_iter + 1][kThreads]: the matrix before each row step
+    const Lane L = lane_of(T);
+    const float rv = L.valid ? r[L.t] : 1.f;
+    const float a_res = alpha[2];
+    const float pres = L.valid ? proj[L.t * 32 + 8 + L.l] : 0.f;
+    const float A0 = res_exp(a_res * pres / rv + bias[8 + L.l]);
+    float A = A0;
+    for (int k = 0; k < n_iter; ++k) {
+        iters[k * kThreads + threadIdx.x] = A;
+        const float R = A / row_sum(A);
+        A = R / col_sum(R);
+    }
+    iters[n_iter * kThreads + threadIdx.x] = A;
+    // reverse mode, last iteration first:
+    //   column step M = R / c:  dR = (dM - sum_i dM M) / c
+    //   row step    R = A / s:  dA = (dR - sum_j dR R) / s
+    float d = L.valid ? grad_h[L.t * kNProj + 8 + L.l] : 0.f;
+    for (int k = n_iter - 1; k >= 0; --k) {
+        const float Ak = iters[k * kThreads + threadIdx.x];
+        const float M = iters[(k + 1) * kThreads + threadIdx.x];
+        const float s = row_sum(Ak);
+        const float R = Ak / s;
+        const float c = col_sum(R);
+        const float dR = (d - col_sum(d * M)) / c;
+        d = (dR - row_sum(dR * R)) / s;
+    }
+    const float dl_res = d * A0;
+    // pre / post gates: sigmoid'(l) = s (1 - s), times 2 for post
+    float dl_g = 0.f, a_g = 0.f, pg = 0.f;
+    if (L.l < 8 && L.valid) {
+        a_g = L.l < 4 ? alpha[0] : alpha[1];
+        pg = proj[L.t * 32 + L.l];
+        const float s = sigmoid(a_g * pg / rv + bias[L.l]);
+        const float gsc = L.l < 4 ? 1.f : 2.f;
+        dl_g = grad_h[L.t * kNProj + L.l] * gsc * s * (1.f - s);
+    }
+    // grad_r = -sum_j dl_j a_j proj_j / r^2 over the token's 24 columns
+    float term = dl_res * a_res * pres + dl_g * a_g * pg;
+    term += __shfl_xor_sync(kFull, term, 1, 16);
+    term += __shfl_xor_sync(kFull, term, 2, 16);
+    term += __shfl_xor_sync(kFull, term, 4, 16);
+    term += __shfl_xor_sync(kFull, term, 8, 16);
+    if (!L.valid) return;
+    float* gp = grad_proj + L.t * 32;
+    gp[8 + L.l] = dl_res * a_res / rv;
+    if (L.l < 8) gp[L.l] = dl_g * a_g / rv;
+    else gp[24 + (L.l - 8)] = 0.f;   // the stored width is 32
+    if (L.l == 0) grad_r[L.t] = -term / (rv * rv);
+    if (dlogits != nullptr) {
+        dlogits[L.t * kNProj + 8 + L.l] = dl_res;
+        if (L.l < 8) dlogits[L.t * kNProj + L.l] = dl_g;
+    }
+}
+
+}  // namespace
+
+size_t backward_smem_bytes(int n_iter) { return (size_t)(n_iter + 1) * kThreads * sizeof(float); }
+
+cudaError_t setup() {
+    return cudaFuncSetAttribute(gate_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)backward_smem_bytes(kMaxIter));
+}
+
+cudaError_t launch_forward(int64_t T, int n_iter, const float* proj, const float* r,
+                           const float* alpha, const float* bias, float* h, cudaStream_t stream) {
+    const unsigned grid = (unsigned)((T + kTokensPerBlock - 1) / kTokensPerBlock);
+    gate_forward_kernel<<<grid, kThreads, 0, stream>>>(T, n_iter, proj, r, alpha, bias, h);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backward(int64_t T, int n_iter, const float* proj, const float* r,
+                            const float* alpha, const float* bias, const float* grad_h,
+                            float* grad_proj, float* grad_r, float* dlogits, cudaStream_t stream) {
+    const unsigned grid = (unsigned)((T + kTokensPerBlock - 1) / kTokensPerBlock);
+    gate_backward_kernel<<<grid, kThreads, backward_smem_bytes(n_iter), stream>>>(
+        T, n_iter, proj, r, alpha, bias, grad_h, grad_proj, grad_r, dlogits);
+    return cudaGetLastError();
+}
+
+}  // namespace gates
+}  // namespace mhcpb

@@ -514,6 +514,90 @@ mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const fl
                         ev_between, ev_after);
 }
 
+// Shared checks of the two gate calls: shape, pointers (device, alignment,
+// overlap of every output with every other operand), per-device set-up.
+static mhcpb_status_t gate_checks(int64_t T, int n_iter, const void* const* in, const size_t* in_sz,
+                                  int n_in, void* const* out, const size_t* out_sz, int n_out) {
+    if (T < 1 || T > MHCPB_MAX_T || n_iter < 1 || n_iter > MHCPB_GATE_MAX_ITER)
+        return MHCPB_ERR_UNSUPPORTED_SHAPE;
+    for (int i = 0; i < n_in; ++i)
+        if (in[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
+    for (int i = 0; i < n_out; ++i)
+        if (out[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
+    for (int i = 0; i < n_in; ++i)
+        if ((reinterpret_cast<uintptr_t>(in[i]) & 3u) != 0) return MHCPB_ERR_MISALIGNED;
+    for (int i = 0; i < n_out; ++i)
+        if ((reinterpret_cast<uintptr_t>(out[i]) & 3u) != 0) return MHCPB_ERR_MISALIGNED;
+    for (int i = 0; i < n_out; ++i) {
+        const Range o{reinterpret_cast<uintptr_t>(out[i]), reinterpret_cast<uintptr_t>(out[i]) + out_sz[i]};
+        for (int j = 0; j < n_in; ++j)
+            if (overlap(o, Range{reinterpret_cast<uintptr_t>(in[j]), reinterpret_cast<uintptr_t>(in[j]) + in_sz[j]}))
+                return MHCPB_ERR_ALIASING;
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlap(o, Range{reinterpret_cast<uintptr_t>(out[j]), reinterpret_cast<uintptr_t>(out[j]) + out_sz[j]}))
+                return MHCPB_ERR_ALIASING;
+    }
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    for (int i = 0; i < n_in; ++i) {
+        mhcpb_status_t s = check_device_ptr(in[i], device);
+        if (s != MHCPB_OK) return s;
+    }
+    for (int i = 0; i < n_out; ++i) {
+        mhcpb_status_t s = check_device_ptr(out[i], device);
+        if (s != MHCPB_OK) return s;
+    }
+    constexpr int kMaxDevices = 64;
+    static std::once_flag once[kMaxDevices];
+    static mhcpb_status_t setup_status[kMaxDevices];
+    if (device < 0 || device >= kMaxDevices) return MHCPB_ERR_INVALID_ARG;
+    std::call_once(once[device], [device] {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) {
+            setup_status[device] = cuda_fail(cudaGetLastError(), "cudaDeviceGetAttribute");
+            return;
+        }
+        if (major != 10 || minor != 3) {
+            setup_status[device] = MHCPB_ERR_UNSUPPORTED_DEVICE;
+            return;
+        }
+        const cudaError_t se = gates::setup();
+        setup_status[device] = se == cudaSuccess ? MHCPB_OK : cuda_fail(se, "setup (gate kernels)");
+    });
+    return setup_status[device];
+}
+
+mhcpb_status_t mhcpb_gate_forward(int64_t T, int n_iter, const float* proj, const float* r,
+                                  const float* alpha, const float* bias, float* h, void* stream) {
+    if (T < 1 || T > MHCPB_MAX_T) return MHCPB_ERR_UNSUPPORTED_SHAPE;
+    const void* in[4] = {proj, r, alpha, bias};
+    const size_t in_sz[4] = {(size_t)T * 32 * 4, (size_t)T * 4, 3 * 4, kNProj * 4};
+    void* out[1] = {h};
+    const size_t out_sz[1] = {(size_t)T * kNProj * 4};
+    mhcpb_status_t s = gate_checks(T, n_iter, in, in_sz, 4, out, out_sz, 1);
+    if (s != MHCPB_OK) return s;
+    cudaError_t e = gates::launch_forward(T, n_iter, proj, r, alpha, bias, h,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MHCPB_OK : cuda_fail(e, "launch (gate forward)");
+}
+
+mhcpb_status_t mhcpb_gate_backward(int64_t T, int n_iter, const float* proj, const float* r,
+                                   const float* alpha, const float* bias, const float* grad_h,
+                                   float* grad_proj, float* grad_r, float* dlogits, void* stream) {
+    if (T < 1 || T > MHCPB_MAX_T) return MHCPB_ERR_UNSUPPORTED_SHAPE;
+    const void* in[5] = {proj, r, alpha, bias, grad_h};
+    const size_t in_sz[5] = {(size_t)T * 32 * 4, (size_t)T * 4, 3 * 4, kNProj * 4, (size_t)T * kNProj * 4};
+    void* out[3] = {grad_proj, grad_r, dlogits};
+    const size_t out_sz[3] = {(size_t)T * 32 * 4, (size_t)T * 4, (size_t)T * kNProj * 4};
+    mhcpb_status_t s = gate_checks(T, n_iter, in, in_sz, 5, out, out_sz, dlogits ? 3 : 2);
+    if (s != MHCPB_OK) return s;
+    cudaError_t e = gates::launch_backward(T, n_iter, proj, r, alpha, bias, grad_h, grad_proj,
+                                           grad_r, dlogits, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MHCPB_OK : cuda_fail(e, "launch (gate backward)");
+}
+
 mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status, int clear) {
     if (plan == nullptr || status == nullptr) return MHCPB_ERR_INVALID_ARG;
     DeviceGuard g(plan->device);

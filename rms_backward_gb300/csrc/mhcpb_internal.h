@@ -122,6 +122,20 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorM
                    cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, cudaEvent_t ev2);
 }  // namespace fwd
 
+// Gate/normalisation step (mhcpb_gate_forward / mhcpb_gate_backward): a
+// half-warp per token; the backward keeps n_iter + 1 matrices per token in
+// shared memory.
+namespace gates {
+constexpr int kMaxIter = 64;
+size_t backward_smem_bytes(int n_iter);
+cudaError_t setup();
+cudaError_t launch_forward(int64_t T, int n_iter, const float* proj, const float* r,
+                           const float* alpha, const float* bias, float* h, cudaStream_t stream);
+cudaError_t launch_backward(int64_t T, int n_iter, const float* proj, const float* r,
+                            const float* alpha, const float* bias, const float* grad_h,
+                            float* grad_proj, float* grad_r, float* dlogits, cudaStream_t stream);
+}  // namespace gates
+
 // Host helpers shared by the entry points (defined in mhcpb_api.cu).
 // encode_tc_maps: the six tensor maps of the tensor-core kernel; returns the
 // name of the map that failed, or null.  record_cuda_error: stores the
