@@ -18,9 +18,11 @@
 // column sum a 2-step shuffle inside the half-warp.  FP32 throughout.  The
 // exponentials are taken after subtracting each row's maximum: the first row
 // normalisation makes the result (and its gradient) independent of any
-// per-row factor, so this changes nothing but the range.  The backward keeps
-// the matrix before each row normalisation in shared memory (one float per
-// lane and iteration) and recomputes the rest on the way back.
+// per-row factor, so this changes nothing but the range.  Each normalisation
+// multiplies by the reciprocal of the sum (__frcp_rn, correctly rounded).  The
+// backward keeps, per lane and iteration, the matrix entry before the row
+// normalisation and the reciprocals of its row and column sums in shared
+// memory, so that going back costs two shuffle reductions per step.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -81,8 +83,8 @@ __global__ void __launch_bounds__(kThreads) gate_forward_kernel(int64_t T, int n
     const float pres = L.valid ? proj[L.t * 32 + 8 + L.l] : 0.f;
     float A = res_exp(alpha[2] * pres / rv + bias[8 + L.l]);
     for (int k = 0; k < n_iter; ++k) {
-        const float R = A / row_sum(A);
-        A = R / col_sum(R);
+        const float R = A * __frcp_rn(row_sum(A));
+        A = R * __frcp_rn(col_sum(R));
     }
     if (!L.valid) return;
     h[L.t * kNProj + 8 + L.l] = A;
@@ -98,7 +100,11 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     const float* __restrict__ alpha, const float* __restrict__ bias,
     const float* __restrict__ grad_h, float* __restrict__ grad_proj, float* __restrict__ grad_r,
     float* __restrict__ dlogits) {
-    extern __shared__ float iters[];   // [n_iter + 1][kThreads]: the matrix before each row step
+    // [n_iter + 1][kThreads] the matrix before each row step, then
+    // [n_iter][kThreads] 1 / row sum and [n_iter][kThreads] 1 / column sum
+    extern __shared__ float iters[];
+    float* rrow = iters + (size_t)(n_iter + 1) * kThreads;
+    float* rcol = rrow + (size_t)n_iter * kThreads;
     const Lane L = lane_of(T);
     const float rv = L.valid ? r[L.t] : 1.f;
     const float a_res = alpha[2];
@@ -107,8 +113,12 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     float A = A0;
     for (int k = 0; k < n_iter; ++k) {
         iters[k * kThreads + threadIdx.x] = A;
-        const float R = A / row_sum(A);
-        A = R / col_sum(R);
+        const float rs = __frcp_rn(row_sum(A));
+        const float R = A * rs;
+        const float rc = __frcp_rn(col_sum(R));
+        rrow[k * kThreads + threadIdx.x] = rs;
+        rcol[k * kThreads + threadIdx.x] = rc;
+        A = R * rc;
     }
     iters[n_iter * kThreads + threadIdx.x] = A;
     // reverse mode, last iteration first:
@@ -116,13 +126,12 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     //   row step    R = A / s:  dA = (dR - sum_j dR R) / s
     float d = L.valid ? grad_h[L.t * kNProj + 8 + L.l] : 0.f;
     for (int k = n_iter - 1; k >= 0; --k) {
-        const float Ak = iters[k * kThreads + threadIdx.x];
+        const float rs = rrow[k * kThreads + threadIdx.x];
+        const float rc = rcol[k * kThreads + threadIdx.x];
+        const float R = iters[k * kThreads + threadIdx.x] * rs;
         const float M = iters[(k + 1) * kThreads + threadIdx.x];
-        const float s = row_sum(Ak);
-        const float R = Ak / s;
-        const float c = col_sum(R);
-        const float dR = (d - col_sum(d * M)) / c;
-        d = (dR - row_sum(dR * R)) / s;
+        const float dR = (d - col_sum(d * M)) * rc;
+        d = (dR - row_sum(dR * R)) * rs;
     }
     const float dl_res = d * A0;
     // pre / post gates: sigmoid'(l) = s (1 - s), times 2 for post
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
 
 }  // namespace
 
-size_t backward_smem_bytes(int n_iter) { return (size_t)(n_iter + 1) * kThreads * sizeof(float); }
+size_t backward_smem_bytes(int n_iter) { return (size_t)(3 * n_iter + 1) * kThreads * sizeof(float); }
 
 cudaError_t setup() {
     return cudaFuncSetAttribute(gate_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
