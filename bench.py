@@ -55,8 +55,10 @@ def _args():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["training_profile", "long_sublayer", "edge", "fused_addend"],
                     help="the headline is the training profile; the others are extra lines")
-    ap.add_argument("--stage", choices=["backward", "forward"], default="backward",
-                    help="backward (the headline) or the stage's forward (proj and r)")
+    ap.add_argument("--stage", choices=["backward", "forward", "gates"], default="backward",
+                    help="backward (the headline), the stage's forward (proj and r), or the "
+                         "gate/normalisation step's backward (grad_proj and grad_r from the "
+                         "gates' gradients) at the workload's T")
     ap.add_argument("--compensated-dw", action="store_true",
                     help="plan flag MHCPB_COMPENSATED_DW (TwoSum dW reduction, one rounding)")
     ap.add_argument("--timing", choices=["block", "flushed"], default="flushed",
@@ -907,6 +909,58 @@ def run_forward(args):
     return 0
 
 
+def run_gates(args):
+    """The gate/normalisation step's backward at the workload's T (one GPU):
+    flushed per-call median over the K timed calls; --quick runs the calls
+    only (for profiler captures)."""
+    import torch
+    from rms_backward_gb300 import mhc_gate_backward
+    rank, world, local = _dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    T = WL.CONFIGS[args.workload]["T"]
+    g = WL.make_gates("bench_gates", T=T, seed=_replica_seed(11, rank))
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    proj, r, al, b, gh = f(g.proj), f(g.r), f(g.alpha), f(g.bias), f(g.grad_h)
+    gp = torch.empty((T, 32), dtype=torch.float32, device=dev)
+    gr = torch.empty((T,), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        mhc_gate_backward(proj, r, al, b, gh, gp, gr, n_iter=20, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1.0)
+        call()
+    torch.cuda.synchronize()
+    if args.quick:
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            call()
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"quick": True, "stage": "gates", "steps": args.steps}), flush=True)
+        return 0
+    times = _step_times(call, flush, args.steps, "flushed", stream)
+    st = _stats_us(times)
+    nbytes = T * (96 + 4 + 96 + 128 + 4)
+    peak, peak_kind = _peaks()
+    gbs = nbytes / (st["median_us"] * 1e-6) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": f"mHC gate/normalisation backward (grad_proj, grad_r) at T={T}, 20 Sinkhorn iterations",
+            "value": st["median_us"], "unit": "us", "higher_is_better": False, "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "dtype": "f32", "data": "synthetic",
+            "flushed": st,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "note": "latency-bound: a serial chain of shuffle reductions per token"},
+            "config": {"workload": f"gates, T={T}", "T": T, "n_iter": 20}}), flush=True)
+    return 0
+
+
 def main():
     args = _args()
     if args.cpu_worker is not None:
@@ -915,6 +969,8 @@ def main():
         return run_reference(args)
     if args.stage == "forward":
         return run_forward(args)
+    if args.stage == "gates":
+        return run_gates(args)
     return run_ours(args)
 
 
