@@ -216,22 +216,23 @@ def run_reference(args):
     rank, world, _ = _dist_env()
     if rank != 0:
         return 0
-    import oracle.mhcpb_oracle as O
+    run_oracle, impl = _oracle_impl()
     T, K = WL.CONFIGS[WORKLOAD]["T"], WL.CONFIGS[WORKLOAD]["K"]
     # calibrate tokens per step against the time budget for warmup + steps
     probe = WL.make("ref_probe", T=64, K=K, seed=77)
+    run_oracle(probe.x, probe.w, probe.grad_proj, probe.grad_r, probe.r)   # first call: set-up
     t0 = time.perf_counter()
-    O.mhc_proj_rms_backward(probe.x, probe.w, probe.grad_proj, probe.grad_r, probe.r)
+    run_oracle(probe.x, probe.w, probe.grad_proj, probe.grad_r, probe.r)
     per_token = (time.perf_counter() - t0) / 64
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
     tok = int(max(1, min(T, budget / max(per_token, 1e-9))))
     wl = WL.make("ref_step", T=tok, K=K, seed=78)
     for _ in range(args.warmup):
-        O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
+        run_oracle(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
     clock = _CpuClock()
     with clock:
         for _ in range(args.steps):
-            O.mhc_proj_rms_backward(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
+            run_oracle(wl.x, wl.w, wl.grad_proj, wl.grad_r, wl.r)
     secs = clock.wall
     gbs = WL.algorithmic_bytes(tok, K) * args.steps / secs / 1e9
     cores = clock.cores()
@@ -242,7 +243,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"training profile T={T} K={K} (4 streams x hidden 5120)",
                    "T": T, "K": K, "sample_tokens_per_step": tok},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "impl": impl,
                          "cores_available": os.cpu_count(), "blas_threads": _cpu_threads(),
                          "sample": f"{tok} tokens x K={K} of the training profile per step"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -435,10 +436,22 @@ def _gates_side(T, flush, stream, peak, reps=100, n_iter=20):
     return out
 
 
+def _oracle_impl():
+    """The oracle the CPU baseline times: the C one (FP64 loops, OpenMP over
+    rows; bit-equal to the numpy oracle) when it is built, else numpy."""
+    try:
+        import oracle.mhcpb_oracle_c as OC
+        OC.load()
+        return OC.mhc_proj_rms_backward, "C (FP64 loops, OpenMP over rows)"
+    except Exception:
+        import oracle.mhcpb_oracle as O
+        return (lambda x, w, gp, gr, r: O.mhc_proj_rms_backward(x, w, gp, gr, r)), "numpy (FP64)"
+
+
 def _cpu_worker(spec):
     """Child process of the CPU baseline: times the oracle on one config with
     the cores the parent left it; prints one JSON line."""
-    import oracle.mhcpb_oracle as O
+    run_oracle, impl = _oracle_impl()
     cfg = json.loads(spec)
     reps, seconds = int(cfg["reps"]), float(cfg["seconds"])
     if cfg["config"] == "tiny":
@@ -455,15 +468,15 @@ def _cpu_worker(spec):
         while clock.wall < seconds or i == 0:
             pc = pieces[i % len(pieces)]
             with clock:
-                O.mhc_proj_rms_backward(pc.x, pc.w, pc.grad_proj, pc.grad_r, pc.r)
+                run_oracle(pc.x, pc.w, pc.grad_proj, pc.grad_r, pc.r)
             nbytes += WL.algorithmic_bytes(pc.T, pc.K)
             done += pc.T
             i += 1
         rates.append(nbytes / clock.wall / 1e9)
         cores.append(clock.cores())
         toks.append(done)
-    print(json.dumps({"gbs": rates, "cores": cores, "tokens": toks, "T_full": T_full, "K": K}),
-          flush=True)
+    print(json.dumps({"gbs": rates, "cores": cores, "tokens": toks, "T_full": T_full, "K": K,
+                      "impl": impl}), flush=True)
     return 0
 
 
@@ -495,12 +508,13 @@ def _cpu_baseline_protocol(T, K, reps=3):
                 out[f"{cfg}_{cores_mode}"] = {"error": (res.stderr or res.stdout)[-300:]}
                 continue
             out[f"{cfg}_{cores_mode}"] = {
+                "impl": d.get("impl"),
                 "median_gbs": float(np.median(d["gbs"])), "runs_gbs": d["gbs"],
                 "cores_busy": float(np.median(d["cores"])), "tokens_per_run": d["tokens"],
                 "seconds_per_run": secs}
     head = out.get("training_all", {})
     return {"value": head.get("median_gbs"), "unit": "GB/s", "cores": head.get("cores_busy"),
-            "kind": "oracle", "nproc": nproc,
+            "kind": "oracle", "impl": head.get("impl"), "nproc": nproc,
             "sample": (f"median of {reps} runs of about 3 s each over 512-token slices of the "
                        f"training profile (T={T}, K={K}), on all {nproc} host cores"),
             "protocol": out}

@@ -64,8 +64,9 @@ def test_oracle_imports_nothing_of_the_cuda_path():
 def test_entry_points_import_the_oracle_only_where_allowed():
     allowed = {
         "__graft_entry__.py": {"smoke"},
-        # _cpu_worker: the child process the CPU-baseline leg starts
-        "bench.py": {"_cpu_worker", "run_reference", "run_forward"},
+        # _oracle_impl: the oracle the CPU-baseline leg (its _cpu_worker child)
+        # and the reference arm time
+        "bench.py": {"_oracle_impl", "run_forward"},
     }
     for name, funcs in allowed.items():
         found = _oracle_imports(os.path.join(ROOT, name))
