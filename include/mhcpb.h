@@ -334,7 +334,9 @@ mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const fl
  * Layouts (all FP32, row-major): proj [T, 32] (columns 24..31 not read), r [T],
  * alpha [3], bias [24], h and grad_h [T, 24], grad_proj [T, 32], grad_r [T].
  * FP32 arithmetic; results within 1e-4 of each token's largest magnitude of
- * the exact values.  1 <= T <= MHCPB_MAX_T, 1 <= n_iter <= MHCPB_GATE_MAX_ITER
+ * the exact values (the backward for logits spanning up to ~35; beyond ~70 the
+ * FP32 backward through the unrolled iterations loses accuracy, though it
+ * stays finite; the forward holds at any spread).  1 <= T <= MHCPB_MAX_T, 1 <= n_iter <= MHCPB_GATE_MAX_ITER
  * (else MHCPB_ERR_UNSUPPORTED_SHAPE).  No plan and no workspace: the calls
  * run on the calling thread's current device, where every pointer must be
  * device memory (MHCPB_ERR_WRONG_DEVICE), 4-byte aligned (MHCPB_ERR_MISALIGNED);

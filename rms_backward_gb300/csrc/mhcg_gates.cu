@@ -15,14 +15,20 @@
 //
 // GB300 layout: a half-warp per token, lane i*4+j owns residual entry (i, j)
 // (and lane g < 8 also pre/post gate g), so every row sum is a 2-step and every
-// column sum a 2-step shuffle inside the half-warp.  FP32 throughout.  The
-// exponentials are taken after subtracting each row's maximum: the first row
-// normalisation makes the result (and its gradient) independent of any
-// per-row factor, so this changes nothing but the range.  Each normalisation
-// multiplies by the reciprocal of the sum (__frcp_rn, correctly rounded).  The
-// backward keeps, per lane and iteration, the matrix entry before the row
-// normalisation and the reciprocals of its row and column sums in shared
-// memory, so that going back costs two shuffle reductions per step.
+// column sum a 2-step shuffle inside the half-warp.  FP32 throughout.
+//
+// The iterations first run directly on exp(l - row maximum), dividing by sums
+// through their correctly rounded reciprocals.  Where a token's sums leave
+// the normal FP32 range (logits ~90 or more apart leave a whole column at 0,
+// or the inputs hold NaN), the warp redoes its tokens on logarithms: a row
+// normalisation is log R = log A - LSE_row(log A), a column normalisation
+// log M = log R - LSE_col(log R), each log-sum-exp taken after subtracting the
+// maximum, so no sum can underflow.  Both give the same R and M up to
+// rounding.  The backward carries the gradient with respect to the logarithms: through
+// a column step g <- g - M colsum(g), through a row step g <- g - R rowsum(g),
+// starting from G_res * M and ending at dL/dl_res -- the chain rule of the
+// normalisations written for log-values, with no division.  It keeps R and M
+// (probabilities in [0, 1]) of every iteration in shared memory.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -69,8 +75,53 @@ __device__ __forceinline__ Lane lane_of(int64_t T) {
     return L;
 }
 
-// exp of this lane's residual logit after subtracting its row's maximum
-__device__ __forceinline__ float res_exp(float lres) { return expf(lres - row_max(lres)); }
+__device__ __forceinline__ float col_max(float v) {
+    v = fmaxf(v, __shfl_xor_sync(kFull, v, 4, 16));
+    v = fmaxf(v, __shfl_xor_sync(kFull, v, 8, 16));
+    return v;
+}
+// one Sinkhorn iteration on this lane's log-value: returns log M, and log R
+// (after the row step) through `lr`
+__device__ __forceinline__ float sinkhorn_step_log(float la, float& lr) {
+    const float m = row_max(la);
+    lr = la - (m + logf(row_sum(expf(la - m))));
+    const float m2 = col_max(lr);
+    return lr - (m2 + logf(col_sum(expf(lr - m2))));
+}
+// a sum the direct iterations can divide by: finite and normal with margin
+__device__ __forceinline__ bool sum_ok(float v) { return v >= 1e-30f && v <= 1e30f; }
+
+// n_iter Sinkhorn iterations of this lane's residual logit l; stores R and M
+// of every iteration when `Rs`/`Ms` are given (stride kThreads); returns the
+// final M.  Warp-uniform: every lane of the warp calls it.
+__device__ __forceinline__ float sinkhorn(float l, int n_iter, float* Rs, float* Ms) {
+    // direct: A = exp(l - row max) in (0, 1]
+    float A = expf(l - row_max(l));
+    bool ok = true;
+    for (int k = 0; k < n_iter; ++k) {
+        const float s = row_sum(A);
+        const float R = A * __frcp_rn(s);
+        const float c = col_sum(R);
+        A = R * __frcp_rn(c);
+        ok = ok && sum_ok(s) && sum_ok(c);
+        if (Rs != nullptr) {
+            Rs[k * kThreads + threadIdx.x] = R;
+            Ms[k * kThreads + threadIdx.x] = A;
+        }
+    }
+    if (!__any_sync(kFull, !ok)) return A;
+    // a sum left the safe range somewhere in this warp: redo on logarithms
+    float la = l;
+    for (int k = 0; k < n_iter; ++k) {
+        float lr;
+        la = sinkhorn_step_log(la, lr);
+        if (Rs != nullptr) {
+            Rs[k * kThreads + threadIdx.x] = expf(lr);
+            Ms[k * kThreads + threadIdx.x] = expf(la);
+        }
+    }
+    return expf(la);
+}
 
 __global__ void __launch_bounds__(kThreads) gate_forward_kernel(int64_t T, int n_iter,
                                                                  const float* __restrict__ proj,
@@ -81,13 +132,9 @@ __global__ void __launch_bounds__(kThreads) gate_forward_kernel(int64_t T, int n
     const Lane L = lane_of(T);
     const float rv = L.valid ? r[L.t] : 1.f;
     const float pres = L.valid ? proj[L.t * 32 + 8 + L.l] : 0.f;
-    float A = res_exp(alpha[2] * pres / rv + bias[8 + L.l]);
-    for (int k = 0; k < n_iter; ++k) {
-        const float R = A * __frcp_rn(row_sum(A));
-        A = R * __frcp_rn(col_sum(R));
-    }
+    const float M = sinkhorn(alpha[2] * pres / rv + bias[8 + L.l], n_iter, nullptr, nullptr);
     if (!L.valid) return;
-    h[L.t * kNProj + 8 + L.l] = A;
+    h[L.t * kNProj + 8 + L.l] = M;
     if (L.l < 8) {
         const float a = L.l < 4 ? alpha[0] : alpha[1];
         const float s = sigmoid(a * proj[L.t * 32 + L.l] / rv + bias[L.l]);
@@ -100,40 +147,25 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     const float* __restrict__ alpha, const float* __restrict__ bias,
     const float* __restrict__ grad_h, float* __restrict__ grad_proj, float* __restrict__ grad_r,
     float* __restrict__ dlogits) {
-    // [n_iter + 1][kThreads] the matrix before each row step, then
-    // [n_iter][kThreads] 1 / row sum and [n_iter][kThreads] 1 / column sum
+    // [n_iter][kThreads] R (after each row step), then [n_iter][kThreads] M
+    // (after each column step)
     extern __shared__ float iters[];
-    float* rrow = iters + (size_t)(n_iter + 1) * kThreads;
-    float* rcol = rrow + (size_t)n_iter * kThreads;
+    float* Rs = iters;
+    float* Ms = iters + (size_t)n_iter * kThreads;
     const Lane L = lane_of(T);
     const float rv = L.valid ? r[L.t] : 1.f;
     const float a_res = alpha[2];
     const float pres = L.valid ? proj[L.t * 32 + 8 + L.l] : 0.f;
-    const float A0 = res_exp(a_res * pres / rv + bias[8 + L.l]);
-    float A = A0;
-    for (int k = 0; k < n_iter; ++k) {
-        iters[k * kThreads + threadIdx.x] = A;
-        const float rs = __frcp_rn(row_sum(A));
-        const float R = A * rs;
-        const float rc = __frcp_rn(col_sum(R));
-        rrow[k * kThreads + threadIdx.x] = rs;
-        rcol[k * kThreads + threadIdx.x] = rc;
-        A = R * rc;
-    }
-    iters[n_iter * kThreads + threadIdx.x] = A;
-    // reverse mode, last iteration first:
-    //   column step M = R / c:  dR = (dM - sum_i dM M) / c
-    //   row step    R = A / s:  dA = (dR - sum_j dR R) / s
-    float d = L.valid ? grad_h[L.t * kNProj + 8 + L.l] : 0.f;
+    const float M = sinkhorn(a_res * pres / rv + bias[8 + L.l], n_iter, Rs, Ms);
+    // reverse mode on log-values, last iteration first (g = dL/dlog M):
+    //   column step log M = log R - LSE_col:  g <- g - M sum_col(g)
+    //   row step    log R = log A - LSE_row:  g <- g - R sum_row(g)
+    float g = (L.valid ? grad_h[L.t * kNProj + 8 + L.l] : 0.f) * M;
     for (int k = n_iter - 1; k >= 0; --k) {
-        const float rs = rrow[k * kThreads + threadIdx.x];
-        const float rc = rcol[k * kThreads + threadIdx.x];
-        const float R = iters[k * kThreads + threadIdx.x] * rs;
-        const float M = iters[(k + 1) * kThreads + threadIdx.x];
-        const float dR = (d - col_sum(d * M)) * rc;
-        d = (dR - row_sum(dR * R)) * rs;
+        g = g - Ms[k * kThreads + threadIdx.x] * col_sum(g);
+        g = g - Rs[k * kThreads + threadIdx.x] * row_sum(g);
     }
-    const float dl_res = d * A0;
+    const float dl_res = g;   // dL / dlog A0 = dL / dlogit
     // pre / post gates: sigmoid'(l) = s (1 - s), times 2 for post
     float dl_g = 0.f, a_g = 0.f, pg = 0.f;
     if (L.l < 8 && L.valid) {
@@ -163,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
 
 }  // namespace
 
-size_t backward_smem_bytes(int n_iter) { return (size_t)(3 * n_iter + 1) * kThreads * sizeof(float); }
+size_t backward_smem_bytes(int n_iter) { return (size_t)(2 * n_iter) * kThreads * sizeof(float); }
 
 cudaError_t setup() {
     return cudaFuncSetAttribute(gate_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -123,8 +123,9 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorM
 }  // namespace fwd
 
 // Gate/normalisation step (mhcpb_gate_forward / mhcpb_gate_backward): a
-// half-warp per token; the backward keeps n_iter + 1 matrices and 2 n_iter
-// reciprocal sums per token in shared memory.
+// half-warp per token; log-domain iterations; the backward keeps the row- and
+// column-normalised matrices of every iteration (2 n_iter per token) in shared
+// memory.
 namespace gates {
 constexpr int kMaxIter = 64;
 size_t backward_smem_bytes(int n_iter);

@@ -150,3 +150,42 @@ def test_chain_gate_backward_into_projection_backward():
     dx, dw = run_gpu(wl)
     st = assert_parity_full(wl, dx, dw, "chain")
     print(f"chain: dX {st[0]} dW {st[1]}")
+
+
+@pytest.mark.parametrize("scale", [5.0, 20.0, 60.0])
+def test_gates_large_logits(scale):
+    """Logits far apart (x5: |l| up to 35; x20: 138; x60: 414): exp of the raw
+    logits leaves whole columns at 0 in FP32 beyond ~90 apart, which the
+    log-domain iterations avoid -- the forward matches the oracle at every
+    scale.  The backward through 20 unrolled iterations amplifies FP32
+    rounding once the logits span ~100 (an FP32 model of the same steps is off
+    by 1e-3 at x10 and completely at x20, while the FP64 map barely moves when
+    its inputs are rounded to FP32), so its parity is checked at x5 and only
+    its finiteness beyond."""
+    wl = WL.make_gates("big", T=999, seed=12)
+    wl.proj = (wl.proj * scale).astype(np.float32)
+    got = _fwd(wl, 20)
+    ok, st = G.check_rows(got, G.gate_forward(wl.proj, wl.r, wl.alpha, wl.bias, 20))
+    assert ok, st
+    gp, gr, dl = _bwd(wl, 20)
+    assert np.all(np.isfinite(gp)) and np.all(np.isfinite(gr)) and np.all(np.isfinite(dl))
+    if scale <= 5.0:
+        rgp, rgr, rdl = G.gate_backward(wl.proj, wl.r, wl.alpha, wl.bias, wl.grad_h, 20)
+        ok, st = G.check_rows(gp[:, :24], rgp[:, :24])
+        print(f"large logits x{scale}: grad_proj {st}")
+        assert ok, st
+
+
+def test_gates_nan_stays_in_its_token():
+    """A NaN logit poisons its own token's outputs (as in the oracle) and no
+    other token's."""
+    wl = WL.make_gates("nan", T=64, seed=13)
+    wl.proj[5, 10] = np.nan
+    got = _fwd(wl, 20)
+    ref = G.gate_forward(wl.proj, wl.r, wl.alpha, wl.bias, 20)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    others = np.ones(64, bool)
+    others[5] = False
+    assert not np.any(np.isnan(got[others]))
+    ok, _ = G.check_rows(got[others], ref[others])
+    assert ok
