@@ -146,3 +146,24 @@ def test_cpu_clock_reports_cores_kept_busy():
     assert c.cores() == 1.0          # nothing timed yet
     c.wall, c.cpu = 2.0, 28.0
     assert c.cores() == 14.0
+
+
+def test_committed_traffic_capture_is_current():
+    """profiles/ncu_traffic.json was taken on the streaming kernel's current
+    sources, so the bench line carries its traffic figures; the SMs' L2
+    writes equal the algorithmic dX + partial writes of the training profile."""
+    import json
+    assert bench._ncu_traffic("tcgen05") is not None
+    d = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))["tcgen05"]
+    T, K = 4096, 20480
+    assert d["algorithmic_write_bytes"] == 2 * T * K + 8 * 24 * K * 4
+    assert bench._ncu_l2_writes("tcgen05") == d["algorithmic_write_bytes"]
+
+
+def test_cpu_worker_line(capsys):
+    """The CPU-baseline child: one JSON line with per-run rates and cores."""
+    import json
+    assert bench._cpu_worker(json.dumps({"config": "tiny", "reps": 2, "seconds": 0.05})) == 0
+    d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert len(d["gbs"]) == 2 and all(v > 0 for v in d["gbs"])
+    assert d["T_full"] == 64 and d["K"] == 512 and d["impl"]
