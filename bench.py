@@ -75,6 +75,8 @@ def _args():
                     help="warm-up and timed steps only (for profiler runs); prints a short line")
     ap.add_argument("--no-forward", action="store_true",
                     help="skip the forward side measurement of the backward line")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the long-sublayer (T=16384) side measurement of the backward line")
     ap.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -448,6 +450,44 @@ def _oracle_impl():
         return (lambda x, w, gp, gr, r: O.mhc_proj_rms_backward(x, w, gp, gr, r)), "numpy (FP64)"
 
 
+def _long_side(lib_abi, flush, stream, peak, reps=50):
+    """The same backward at the long sublayer (T=16384, K=20480): flushed
+    per-step median.  Its fixed per-step costs (launch, ramp-up, drain, the
+    reduction) weigh four times less than at the training profile."""
+    import torch
+    from rms_backward_gb300 import Plan
+    cfg = dict(WL.CONFIGS["long_sublayer"])
+    T, K = cfg["T"], cfg["K"]
+    wl = WL.make("long_sublayer", **cfg)
+    dev = flush.device
+    x = torch.from_numpy(wl.x.view(np.int16)).view(torch.bfloat16).to(dev)
+    w, gp = torch.from_numpy(wl.w).to(dev), torch.from_numpy(wl.grad_proj).to(dev)
+    gr, r = torch.from_numpy(wl.grad_r).to(dev), torch.from_numpy(wl.r).to(dev)
+    del wl
+    plan = Plan(T, K, dev.index or 0)
+    dx = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((24, K), dtype=torch.float32, device=dev)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    sh = stream.cuda_stream
+
+    def step():
+        lib_abi.mhcpb_execute(plan.handle, x.data_ptr(), w.data_ptr(), gp.data_ptr(), gr.data_ptr(),
+                              r.data_ptr(), dx.data_ptr(), dw.data_ptr(), ws.data_ptr(),
+                              plan.workspace_bytes, None, sh)
+
+    for _ in range(5):
+        flush.fill_(1.0)
+        step()
+    st = _stats_us(_step_times(step, flush, reps, "flushed", stream))
+    if plan.device_status() != 0:
+        raise RuntimeError("device-side timeout at the long sublayer")
+    plan.close()
+    alg = WL.algorithmic_bytes(T, K)
+    gbs = alg / (st["median_us"] * 1e-6) / 1e9
+    return dict(st, T=T, K=K, value=gbs, unit="GB/s", pct_of_hbm_peak=100.0 * gbs / peak,
+                how=_l2_note("flushed", 2 * T * K, None))
+
+
 def _cpu_worker(spec):
     """Child process of the CPU baseline: times the oracle on one config with
     the cores the parent left it; prints one JSON line."""
@@ -743,6 +783,10 @@ def run_ours(args):
     if not args.no_forward and not has_add:
         fwd = _forward_side(plan, x, w, flush, stream, T, K, peak)
         gates = _gates_side(T, flush, stream, peak)
+    long_sub = None
+    if not args.no_long and args.workload == WORKLOAD and args.kernel == "tcgen05" and rank == 0 \
+            and world == 1:
+        long_sub = _long_side(abi, flush, stream, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
@@ -785,6 +829,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": k1_bytes},
             "forward": fwd,
             "gates": gates,
+            "long_sublayer": long_sub,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "how": "pinned host inputs copied in and dX, dW copied out every step; steps "
