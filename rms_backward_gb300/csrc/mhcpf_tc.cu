@@ -443,50 +443,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // proj[t][j] = sum over chunks ascending of partial[fc][j][t]; r from the
-// summed squares.  Thread = (partial row j' in 0..24, token t); a warp reads
-// 128 contiguous bytes of a chunk's row per load.
-constexpr int kReduceThreads = 256;
+// summed squares.  Block = 32 tokens: warp j' reads partial row j' (24 = sum
+// of squares), lane = token, so each load is one 128-byte line of a chunk's
+// row; the sums meet in shared memory and leave as whole proj rows (a token's
+// 32 floats are one 128-byte line).  Writing 4-byte pieces of 32 different
+// proj rows per warp instead (one thread per output) cost 1.9 us per forward
+// step: each piece is a partial write of a line not in L2.
+constexpr int kReduceTokens = 32;
+constexpr int kReduceThreads = kPartRows * 32;   // 800
 constexpr int kGroup = 40;   // chunk partials loaded before they are summed (all of them at K = 20480)
 
 __global__ void __launch_bounds__(kReduceThreads)
     fwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ proj,
                       float* __restrict__ r, int T, int t_pad, int n_fc, float kf, float eps,
                       int discard) {
+    __shared__ float sums[kPartRows][kReduceTokens + 1];
     ptx::grid_launch_dependents();   // the next forward's kernel 1 may be scheduled
     ptx::grid_dependency_wait();
-    const int64_t i = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x;
-    const bool valid = i < (int64_t)kPartRows * t_pad;   // t_pad % 32 == 0: whole warps
-    const int row = valid ? (int)(i / t_pad) : 0;       // j' (24 = sum of squares)
-    const int t = valid ? (int)(i - (int64_t)row * t_pad) : 0;
+    const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kReduceTokens;   // gridDim.x = t_pad / 32: t0 + lane < t_pad
     const int64_t stride = (int64_t)kPartRows * t_pad;   // floats per chunk
-    const int64_t base = (int64_t)row * t_pad + t;
+    const float* src = part + (int64_t)row * t_pad + t0;
     float a = 0.f;
-    for (int f0 = 0; valid && f0 < n_fc; f0 += kGroup) {
+    for (int f0 = 0; f0 < n_fc; f0 += kGroup) {
         float b[kGroup];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
-            if (f0 + g < n_fc) b[g] = part[(int64_t)(f0 + g) * stride + base];
+            if (f0 + g < n_fc) b[g] = src[(int64_t)(f0 + g) * stride + lane];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
             if (f0 + g < n_fc) a = (f0 + g == 0) ? b[g] : a + b[g];
     }
-    if (valid && t < T) {
-        if (row < kNProj) {
-            proj[(size_t)t * kProjCols + row] = a;
-        } else {
-            r[t] = sqrtf(a / kf + eps);   // the mean of the squares, eps, root
-            float4* pad = reinterpret_cast<float4*>(proj + (size_t)t * kProjCols + kNProj);
-            pad[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            pad[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
-    // the partials are dead once read: drop their L2 lines (a line is one
-    // chunk's row for the 32 tokens of this warp)
+    sums[row][lane] = a;
+    // the partials are dead once read: drop the warp's line of every chunk
+    // from L2, spread over the lanes
     __syncwarp();
-    if (valid && discard) {
-        // the warp's line of each chunk (32 tokens of one row), spread over the lanes
-        const int64_t b0 = base - (t & 31);
-        for (int f = t & 31; f < n_fc; f += 32) ptx::discard_l2_line(part + (int64_t)f * stride + b0);
+    if (discard)
+        for (int f = lane; f < n_fc; f += 32) ptx::discard_l2_line(src + (int64_t)f * stride);
+    __syncthreads();
+    if (threadIdx.x < kReduceTokens * kProjCols / 4) {
+        // 32 proj rows x 8 float4: columns 24..31 are the zero pad
+        const int tt = threadIdx.x >> 3, c = (threadIdx.x & 7) * 4;
+        const int t = t0 + tt;
+        if (t < T) {
+            float4 v;
+            v.x = c + 0 < kNProj ? sums[c + 0][tt] : 0.f;
+            v.y = c + 1 < kNProj ? sums[c + 1][tt] : 0.f;
+            v.z = c + 2 < kNProj ? sums[c + 2][tt] : 0.f;
+            v.w = c + 3 < kNProj ? sums[c + 3][tt] : 0.f;
+            *reinterpret_cast<float4*>(proj + (size_t)t * kProjCols + c) = v;
+        }
+    } else if (threadIdx.x < kReduceTokens * kProjCols / 4 + kReduceTokens) {
+        const int tt = threadIdx.x - kReduceTokens * kProjCols / 4;
+        const int t = t0 + tt;
+        if (t < T) r[t] = sqrtf(sums[kNProj][tt] / kf + eps);   // the mean of the squares, eps, root
     }
 }
 
@@ -517,11 +527,10 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorM
         if ((e = cudaLaunchKernelEx(&cfg, fwd_tc_kernel, p, x_map, w_map)) != cudaSuccess) return e;
     }
     if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return e;
-    const int64_t n = (int64_t)kPartRows * p.t_pad;
     // discard needs 128-byte lines: t_pad is a multiple of 32 floats
     const int discard = (reinterpret_cast<uintptr_t>(p.partial) & 127u) == 0 ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((n + kReduceThreads - 1) / kReduceThreads));
+    cfg.gridDim = dim3((unsigned)(p.t_pad / kReduceTokens));
     cfg.blockDim = dim3(kReduceThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
