@@ -37,10 +37,10 @@
 //    and at the end of each unit the drain of the accumulator; they write
 //    the unit's partials (24 projections and the sum of squares per token)
 //    to the workspace.
-// Kernel 2 sums each token's partials over the chunks in ascending order and
-// writes proj and r (programmatic dependent launch, like the backward's
-// reduction), then drops the dead partial lines from L2.  Every mbarrier wait
-// is bounded (wait_bar).
+// Kernel 2 (one of two layouts, the same bits) sums each token's partials
+// over the chunks in ascending order and writes proj and r (programmatic
+// dependent launch, like the backward's reduction), then drops the dead
+// partial lines from L2.  Every mbarrier wait is bounded (wait_bar).
 #include <cuda_bf16.h>
 
 #include "mhcpb_internal.h"
@@ -443,45 +443,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // proj[t][j] = sum over chunks ascending of partial[fc][j][t]; r from the
-// summed squares.  Block = 32 tokens: warp j' reads partial row j' (24 = sum
-// of squares), lane = token, so each load is one 128-byte line of a chunk's
-// row; the sums meet in shared memory and leave as whole proj rows (a token's
-// 32 floats are one 128-byte line).  Writing 4-byte pieces of 32 different
-// proj rows per warp instead (one thread per output) cost 1.9 us per forward
-// step: each piece is a partial write of a line not in L2.
-constexpr int kReduceTokens = 32;
-constexpr int kReduceThreads = kPartRows * 32;   // 800
+// summed squares.  Two kernels with the same sums in the same order (so the
+// same bits), chosen per call by the number of 32-token blocks:
+//  * lines (at most one block per SM): block = 32 tokens, warp j' sums
+//    partial row j' (lane = token, each load one 128-byte line), and the sums
+//    leave through shared memory as whole proj rows (a token's 32 floats are
+//    one 128-byte line).  68 registers x 800 threads: one block per SM;
+//  * outputs (more blocks than SMs): thread = (row j', token t), 256-thread
+//    blocks, several per SM.  Its warps write 4-byte pieces of 32 proj rows
+//    each, which costs ~1.7 us per call at T = 4096; but it keeps more loads
+//    in flight per SM, and at T = 16384 it is ~1.7 us faster than lines in
+//    3.4 waves.
 constexpr int kGroup = 40;   // chunk partials loaded before they are summed (all of them at K = 20480)
+constexpr int kLineTokens = 32;
+constexpr int kLineThreads = kPartRows * 32;   // 800
+constexpr int kOutThreads = 256;
 
-__global__ void __launch_bounds__(kReduceThreads)
-    fwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ proj,
-                      float* __restrict__ r, int T, int t_pad, int n_fc, float kf, float eps,
-                      int discard) {
-    __shared__ float sums[kPartRows][kReduceTokens + 1];
-    ptx::grid_launch_dependents();   // the next forward's kernel 1 may be scheduled
-    ptx::grid_dependency_wait();
-    const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.x * kReduceTokens;   // gridDim.x = t_pad / 32: t0 + lane < t_pad
-    const int64_t stride = (int64_t)kPartRows * t_pad;   // floats per chunk
-    const float* src = part + (int64_t)row * t_pad + t0;
+// the ascending-order sum over the chunks of one partial element (src points
+// at chunk 0; stride floats per chunk), every group's loads in flight together
+__device__ __forceinline__ float sum_chunks(const float* src, int64_t stride, int n_fc) {
     float a = 0.f;
     for (int f0 = 0; f0 < n_fc; f0 += kGroup) {
         float b[kGroup];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
-            if (f0 + g < n_fc) b[g] = src[(int64_t)(f0 + g) * stride + lane];
+            if (f0 + g < n_fc) b[g] = src[(int64_t)(f0 + g) * stride];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
             if (f0 + g < n_fc) a = (f0 + g == 0) ? b[g] : a + b[g];
     }
-    sums[row][lane] = a;
+    return a;
+}
+
+__global__ void __launch_bounds__(kLineThreads)
+    fwd_reduce_lines_kernel(const float* __restrict__ part, float* __restrict__ proj,
+                            float* __restrict__ r, int T, int t_pad, int n_fc, float kf, float eps,
+                            int discard) {
+    __shared__ float sums[kPartRows][kLineTokens + 1];
+    ptx::grid_launch_dependents();   // the next forward's kernel 1 may be scheduled
+    ptx::grid_dependency_wait();
+    const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * kLineTokens;   // gridDim.x = t_pad / 32: t0 + lane < t_pad
+    const int64_t stride = (int64_t)kPartRows * t_pad;   // floats per chunk
+    const float* src = part + (int64_t)row * t_pad + t0;
+    sums[row][lane] = sum_chunks(src + lane, stride, n_fc);
     // the partials are dead once read: drop the warp's line of every chunk
     // from L2, spread over the lanes
     __syncwarp();
     if (discard)
         for (int f = lane; f < n_fc; f += 32) ptx::discard_l2_line(src + (int64_t)f * stride);
     __syncthreads();
-    if (threadIdx.x < kReduceTokens * kProjCols / 4) {
+    if (threadIdx.x < kLineTokens * kProjCols / 4) {
         // 32 proj rows x 8 float4: columns 24..31 are the zero pad
         const int tt = threadIdx.x >> 3, c = (threadIdx.x & 7) * 4;
         const int t = t0 + tt;
@@ -493,10 +505,41 @@ __global__ void __launch_bounds__(kReduceThreads)
             v.w = c + 3 < kNProj ? sums[c + 3][tt] : 0.f;
             *reinterpret_cast<float4*>(proj + (size_t)t * kProjCols + c) = v;
         }
-    } else if (threadIdx.x < kReduceTokens * kProjCols / 4 + kReduceTokens) {
-        const int tt = threadIdx.x - kReduceTokens * kProjCols / 4;
+    } else if (threadIdx.x < kLineTokens * kProjCols / 4 + kLineTokens) {
+        const int tt = threadIdx.x - kLineTokens * kProjCols / 4;
         const int t = t0 + tt;
         if (t < T) r[t] = sqrtf(sums[kNProj][tt] / kf + eps);   // the mean of the squares, eps, root
+    }
+}
+
+__global__ void __launch_bounds__(kOutThreads)
+    fwd_reduce_outputs_kernel(const float* __restrict__ part, float* __restrict__ proj,
+                              float* __restrict__ r, int T, int t_pad, int n_fc, float kf,
+                              float eps, int discard) {
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
+    const int64_t i = (int64_t)blockIdx.x * kOutThreads + threadIdx.x;
+    const bool valid = i < (int64_t)kPartRows * t_pad;   // t_pad % 32 == 0: whole warps
+    const int row = valid ? (int)(i / t_pad) : 0;       // j' (24 = sum of squares)
+    const int t = valid ? (int)(i - (int64_t)row * t_pad) : 0;
+    const int64_t stride = (int64_t)kPartRows * t_pad;
+    const int64_t base = (int64_t)row * t_pad + t;
+    const float a = valid ? sum_chunks(part + base, stride, n_fc) : 0.f;
+    if (valid && t < T) {
+        if (row < kNProj) {
+            proj[(size_t)t * kProjCols + row] = a;
+        } else {
+            r[t] = sqrtf(a / kf + eps);
+            float4* pad = reinterpret_cast<float4*>(proj + (size_t)t * kProjCols + kNProj);
+            pad[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            pad[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    // the warp's line of each chunk (32 tokens of one row), spread over the lanes
+    __syncwarp();
+    if (valid && discard) {
+        const int64_t b0 = base - (t & 31);
+        for (int f = t & 31; f < n_fc; f += 32) ptx::discard_l2_line(part + (int64_t)f * stride + b0);
     }
 }
 
@@ -529,9 +572,13 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorM
     if (ev1 && (e = cudaEventRecord(ev1, stream)) != cudaSuccess) return e;
     // discard needs 128-byte lines: t_pad is a multiple of 32 floats
     const int discard = (reinterpret_cast<uintptr_t>(p.partial) & 127u) == 0 ? 1 : 0;
+    // one wave of line blocks (kernel 1's grid is the SM count unless the
+    // problem has fewer units, or a cap lowers it), else the output threads
+    const bool lines = p.t_pad / kLineTokens <= grid;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.t_pad / kReduceTokens));
-    cfg.blockDim = dim3(kReduceThreads);
+    cfg.gridDim = lines ? dim3((unsigned)(p.t_pad / kLineTokens))
+                        : dim3((unsigned)(((int64_t)kPartRows * p.t_pad + kOutThreads - 1) / kOutThreads));
+    cfg.blockDim = dim3(lines ? kLineThreads : kOutThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -539,9 +586,9 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorM
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, fwd_reduce_kernel, static_cast<const float*>(p.partial),
-                                p.proj, p.r, p.T, p.t_pad, p.n_fc, (float)p.K, p.eps, discard)) !=
-        cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, lines ? fwd_reduce_lines_kernel : fwd_reduce_outputs_kernel,
+                                static_cast<const float*>(p.partial), p.proj, p.r, p.T, p.t_pad,
+                                p.n_fc, (float)p.K, p.eps, discard)) != cudaSuccess)
         return e;
     if (ev2 && (e = cudaEventRecord(ev2, stream)) != cudaSuccess) return e;
     return cudaSuccess;

@@ -104,6 +104,10 @@ def test_zero_rows_and_eps():
 
 
 def test_bitwise_repeatable_and_grid_independent():
+    """Kernel 1's unit boundaries depend only on (T, K), and the reduction's
+    two layouts sum in the same order: T = 1537 makes 49 blocks of 32 tokens,
+    so caps 1 and 5 run the output-thread reduction and caps 77 and none the
+    line reduction; every result has the same bits."""
     wl = WL.make("f", T=1537, K=5128, seed=74)
     outs = [run_forward(wl, cap=c) for c in (0, 1, 5, 77, 0)]
     for p, r in outs[1:]:
