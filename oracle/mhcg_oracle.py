@@ -155,7 +155,7 @@ def check_rows(got, ref, rel=1e-4, floor=1e-30):
     scale = np.max(np.abs(np.where(np.isfinite(r), r, 0.0)), axis=1, keepdims=True)
     lim = rel * scale + floor
     fin = np.isfinite(r)
-    diff = np.abs(np.where(fin, g - r, 0.0))
+    diff = np.abs(np.subtract(g, r, out=np.zeros_like(g), where=fin))   # 0 where ref is not finite
     ok = np.where(fin, (diff <= lim) & np.isfinite(g), (np.isnan(g) & np.isnan(r)) | (g == r))
     worst = float(np.max(np.where(fin, diff / lim, 0.0))) if r.size else 0.0
     return bool(ok.all()), dict(n=int(r.size), fail=int((~ok).sum()), worst_frac_of_tol=worst)

@@ -241,7 +241,7 @@ def check_dx(dx_bits, ref_bits, abs_bound, ulps=2.0, rel_abs=2.0 ** -16):
     b = bf16_bits_to_f64(ref_bits)
     fin = np.isfinite(b)
     same_nonfinite = (~fin) & ((np.isnan(a) & np.isnan(b)) | (a == b))
-    diff = np.abs(np.where(fin, a - b, 0.0))
+    diff = np.abs(np.subtract(a, b, out=np.zeros_like(a), where=fin))   # 0 where ref is not finite
     u = bf16_ulp(b)
     pass_ulp = diff <= ulps * u
     pass_abs = diff <= u + rel_abs * np.asarray(abs_bound)
@@ -282,7 +282,7 @@ def check_dx_addend(dx_bits, ref_bits, core_ref_bits, core_abs_bound, ulps=2.0,
     b = bf16_bits_to_f64(ref_bits)
     core = bf16_bits_to_f64(core_ref_bits)
     fin = np.isfinite(b)
-    diff = np.abs(np.where(fin, a - b, 0.0))
+    diff = np.abs(np.subtract(a, b, out=np.zeros_like(a), where=fin))   # 0 where ref is not finite
     u = bf16_ulp(b)
     lim = np.maximum(ulps * u, ulps * bf16_ulp(core) + rel_abs * np.asarray(core_abs_bound) + u)
     ok_elem = np.where(fin, (diff <= lim) & np.isfinite(a), (np.isnan(a) & np.isnan(b)) | (a == b))
