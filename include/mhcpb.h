@@ -62,7 +62,7 @@ typedef struct mhcpb_plan_s* mhcpb_plan_t;
 typedef enum {
     MHCPB_OK = 0,
     MHCPB_ERR_INVALID_ARG = 1,        /* NULL plan/pointer, addend presence disagreeing with the plan */
-    MHCPB_ERR_UNSUPPORTED_SHAPE = 2,  /* T < 1, K not a positive multiple of 8, or above the maxima below */
+    MHCPB_ERR_UNSUPPORTED_SHAPE = 2,  /* T < 0, K not a positive multiple of 8, or above the maxima below */
     MHCPB_ERR_MISALIGNED = 3,         /* a pointer not 16-byte aligned */
     MHCPB_ERR_ALIASING = 4,           /* two operands (or workspace) share bytes */
     MHCPB_ERR_WRONG_DEVICE = 5,       /* a pointer not in device memory of the plan's device */
@@ -118,7 +118,13 @@ enum {
     MHCPB_TEST_INJECT_STALL = 1u << 30
 };
 
-/* Shape limits (inclusive). */
+/* Shape limits (inclusive).  0 <= T <= MHCPB_MAX_T.  T = 0 (an empty batch)
+ * is valid everywhere: dX, proj, r and the gate outputs are empty, dW (a sum
+ * over no tokens) is written as zeros, or left as dW + 0 with
+ * MHCPB_ACCUMULATE_DW, and the workspaces are 0 bytes.  An operand with no
+ * elements needs no storage: its pointer may be NULL and is not checked;
+ * every non-empty operand (W, dW, the gates' alpha and bias) is checked as
+ * for T > 0. */
 #define MHCPB_MAX_T (1 << 24)
 #define MHCPB_MAX_K (1 << 20)
 /* Number of projection columns used, stored width of grad_proj. */
@@ -336,7 +342,7 @@ mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const fl
  * FP32 arithmetic; results within 1e-4 of each token's largest magnitude of
  * the exact values (the backward for logits spanning up to ~35; beyond ~70 the
  * FP32 backward through the unrolled iterations loses accuracy, though it
- * stays finite; the forward holds at any spread).  1 <= T <= MHCPB_MAX_T, 1 <= n_iter <= MHCPB_GATE_MAX_ITER
+ * stays finite; the forward holds at any spread).  0 <= T <= MHCPB_MAX_T, 1 <= n_iter <= MHCPB_GATE_MAX_ITER
  * (else MHCPB_ERR_UNSUPPORTED_SHAPE).  No plan and no workspace: the calls
  * run on the calling thread's current device, where every pointer must be
  * device memory (MHCPB_ERR_WRONG_DEVICE), 4-byte aligned (MHCPB_ERR_MISALIGNED);

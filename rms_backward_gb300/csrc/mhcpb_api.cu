@@ -136,7 +136,10 @@ const char* encode_maps(CUtensorMap (&m)[6], int64_t T, int64_t K, const void* x
 struct Range {
     uintptr_t lo, hi;
 };
-bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+// an empty range overlaps nothing
+bool overlap(const Range& a, const Range& b) {
+    return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
 
 mhcpb_status_t check_device_ptr(const void* ptr, int device) {
     cudaPointerAttributes a;
@@ -192,7 +195,7 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
                             MHCPB_COMPENSATED_DW | MHCPB_ACCUMULATE_DW |
                             MHCPB_TEST_INJECT_STALL)) != 0)
         return MHCPB_ERR_INVALID_ARG;
-    if (T < 1 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
+    if (T < 0 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
         return MHCPB_ERR_UNSUPPORTED_SHAPE;
     if (device < 0) return MHCPB_ERR_INVALID_ARG;
 
@@ -256,10 +259,11 @@ mhcpb_status_t mhcpb_plan_create(mhcpb_plan_t* out, int64_t T, int64_t K, int de
         delete p;
         return cuda_fail(e, "cudaMemset (status word)");
     }
-    if (!fma_kernel) {
+    if (!fma_kernel && T > 0) {
         // The tensor maps depend on the execute's pointers, but their shapes
         // can be checked now: encode them over a real device address (the
         // status word; encoding records the address and reads nothing).
+        // T = 0 launches no streaming kernel and needs no map.
         CUtensorMap m[6];
         const void* a = p->d_status;
         if (const char* bad = encode_maps(m, T, K, a, a, a, a, a, a)) {
@@ -315,15 +319,10 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, int what, const void* x, c
     if (plan == nullptr) return MHCPB_ERR_INVALID_ARG;
     const bool run1 = (what & kRunStream) != 0, run2 = (what & kRunReduce) != 0;
     const bool add = (plan->flags & MHCPB_HAS_ADDEND) != 0;
-    if (!workspace) return MHCPB_ERR_INVALID_ARG;
-    if (run1 && (!x || !w || !grad_proj || !grad_r || !r || !dx)) return MHCPB_ERR_INVALID_ARG;
-    if (run1 && add != (grad_x_addend != nullptr)) return MHCPB_ERR_INVALID_ARG;
-    if (run2 && !dw) return MHCPB_ERR_INVALID_ARG;
-    if (workspace_bytes < plan->ws_bytes) return MHCPB_ERR_WORKSPACE_TOO_SMALL;
-
     const int64_t T = plan->T, K = plan->K;
     // operands of the kernels that run: 0..5 kernel 1's inputs and dX, 6 dW,
-    // 7 the workspace, 8 the addend
+    // 7 the workspace, 8 the addend.  An operand with no elements (at T = 0:
+    // all but W and dW) needs no storage and its pointer is not checked.
     const void* all[9] = {x, w, grad_proj, grad_r, r, dx, dw, workspace, grad_x_addend};
     const size_t all_sizes[9] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4),
                                  (size_t)(T * kGradProjCols * 4), (size_t)(T * 4), (size_t)(T * 4),
@@ -334,11 +333,13 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, int what, const void* x, c
     int n = 0;
     for (int i = 0; i < 9; ++i) {
         const bool used = (i <= 5) ? run1 : (i == 6) ? run2 : (i == 7) ? true : (run1 && add);
-        if (used) {
-            ptrs[n] = all[i];
-            sizes[n++] = all_sizes[i];
-        }
+        if (!used || all_sizes[i] == 0) continue;
+        if (all[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
+        ptrs[n] = all[i];
+        sizes[n++] = all_sizes[i];
     }
+    if (run1 && T > 0 && add != (grad_x_addend != nullptr)) return MHCPB_ERR_INVALID_ARG;
+    if (workspace_bytes < plan->ws_bytes) return MHCPB_ERR_WORKSPACE_TOO_SMALL;
     for (int i = 0; i < n; ++i)
         if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != 0) return MHCPB_ERR_MISALIGNED;
     Range rg[9];
@@ -361,7 +362,7 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, int what, const void* x, c
     cudaError_t e;
     if (ev0 && (e = cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev0), st)) != cudaSuccess)
         return cuda_fail(e, "cudaEventRecord");
-    if (run1) {
+    if (run1 && T > 0) {   // T = 0: no dX, no partials
         MainParams p{};
         p.T = (int32_t)T;
         p.K = (int32_t)K;
@@ -397,7 +398,8 @@ static mhcpb_status_t execute_impl(mhcpb_plan_t plan, int what, const void* x, c
         return cuda_fail(e, "cudaEventRecord");
     if (run2) {
         // partials written by this same call are dead after the sum (their L2
-        // lines may be dropped); a stand-alone reduction leaves them intact
+        // lines may be dropped); a stand-alone reduction leaves them intact.
+        // At T = 0 there are none (S = 0): dW = 0, or dW + 0 when accumulating
         e = launch_reduce(static_cast<const float*>(workspace), dw, plan->S, (int64_t)kNProj * K,
                           (plan->flags & MHCPB_COMPENSATED_DW) != 0,
                           (plan->flags & MHCPB_ACCUMULATE_DW) != 0, run1, st);
@@ -448,28 +450,40 @@ mhcpb_status_t mhcpb_forward_workspace_bytes(mhcpb_plan_t plan, size_t* bytes) {
 static mhcpb_status_t forward_impl(mhcpb_plan_t plan, const void* x, const float* w, float eps,
                                    float* proj, float* r, void* workspace, size_t workspace_bytes,
                                    void* stream, void* ev0, void* ev1, void* ev2) {
-    if (plan == nullptr || !x || !w || !proj || !r || !workspace) return MHCPB_ERR_INVALID_ARG;
-    if (!(eps >= 0.f) || !(eps < INFINITY)) return MHCPB_ERR_INVALID_ARG;
+    if (plan == nullptr) return MHCPB_ERR_INVALID_ARG;
     const int64_t T = plan->T, K = plan->K;
     const size_t ws = fwd::workspace_bytes(T, K);
+    // an operand with no elements (at T = 0: all but W) needs no storage and
+    // its pointer is not checked
+    const void* all[5] = {x, w, proj, r, workspace};
+    const size_t all_sizes[5] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4),
+                                 (size_t)(T * fwd::kProjCols * 4), (size_t)(T * 4), ws};
+    const void* ptrs[5];
+    size_t sizes[5];
+    int n = 0;
+    for (int i = 0; i < 5; ++i) {
+        if (all_sizes[i] == 0) continue;
+        if (all[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
+        ptrs[n] = all[i];
+        sizes[n++] = all_sizes[i];
+    }
+    if (!(eps >= 0.f) || !(eps < INFINITY)) return MHCPB_ERR_INVALID_ARG;
     if (workspace_bytes < ws) return MHCPB_ERR_WORKSPACE_TOO_SMALL;
-    const void* ptrs[5] = {x, w, proj, r, workspace};
-    const size_t sizes[5] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4),
-                             (size_t)(T * fwd::kProjCols * 4), (size_t)(T * 4), ws};
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < n; ++i)
         if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != 0) return MHCPB_ERR_MISALIGNED;
     Range rg[5];
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < n; ++i) {
         rg[i].lo = reinterpret_cast<uintptr_t>(ptrs[i]);
         rg[i].hi = rg[i].lo + sizes[i];
     }
-    for (int i = 0; i < 5; ++i)
-        for (int j = i + 1; j < 5; ++j)
+    for (int i = 0; i < n; ++i)
+        for (int j = i + 1; j < n; ++j)
             if (overlap(rg[i], rg[j])) return MHCPB_ERR_ALIASING;
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < n; ++i) {
         mhcpb_status_t s = check_device_ptr(ptrs[i], plan->device);
         if (s != MHCPB_OK) return s;
     }
+    if (T == 0) return MHCPB_OK;   // no tokens: nothing to write
     if (!get_encode()) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
     DeviceGuard g(plan->device);
     if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
@@ -518,16 +532,18 @@ mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const fl
 // overlap of every output with every other operand), per-device set-up.
 static mhcpb_status_t gate_checks(int64_t T, int n_iter, const void* const* in, const size_t* in_sz,
                                   int n_in, void* const* out, const size_t* out_sz, int n_out) {
-    if (T < 1 || T > MHCPB_MAX_T || n_iter < 1 || n_iter > MHCPB_GATE_MAX_ITER)
+    if (T < 0 || T > MHCPB_MAX_T || n_iter < 1 || n_iter > MHCPB_GATE_MAX_ITER)
         return MHCPB_ERR_UNSUPPORTED_SHAPE;
+    // an operand with no elements (at T = 0: all but alpha and bias) needs no
+    // storage and its pointer is not checked; its range is empty below
     for (int i = 0; i < n_in; ++i)
-        if (in[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
+        if (in_sz[i] > 0 && in[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
     for (int i = 0; i < n_out; ++i)
-        if (out[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
+        if (out_sz[i] > 0 && out[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
     for (int i = 0; i < n_in; ++i)
-        if ((reinterpret_cast<uintptr_t>(in[i]) & 3u) != 0) return MHCPB_ERR_MISALIGNED;
+        if (in_sz[i] > 0 && (reinterpret_cast<uintptr_t>(in[i]) & 3u) != 0) return MHCPB_ERR_MISALIGNED;
     for (int i = 0; i < n_out; ++i)
-        if ((reinterpret_cast<uintptr_t>(out[i]) & 3u) != 0) return MHCPB_ERR_MISALIGNED;
+        if (out_sz[i] > 0 && (reinterpret_cast<uintptr_t>(out[i]) & 3u) != 0) return MHCPB_ERR_MISALIGNED;
     for (int i = 0; i < n_out; ++i) {
         const Range o{reinterpret_cast<uintptr_t>(out[i]), reinterpret_cast<uintptr_t>(out[i]) + out_sz[i]};
         for (int j = 0; j < n_in; ++j)
@@ -541,10 +557,12 @@ static mhcpb_status_t gate_checks(int64_t T, int n_iter, const void* const* in, 
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     for (int i = 0; i < n_in; ++i) {
+        if (in_sz[i] == 0) continue;
         mhcpb_status_t s = check_device_ptr(in[i], device);
         if (s != MHCPB_OK) return s;
     }
     for (int i = 0; i < n_out; ++i) {
+        if (out_sz[i] == 0) continue;
         mhcpb_status_t s = check_device_ptr(out[i], device);
         if (s != MHCPB_OK) return s;
     }
@@ -571,13 +589,13 @@ static mhcpb_status_t gate_checks(int64_t T, int n_iter, const void* const* in, 
 
 mhcpb_status_t mhcpb_gate_forward(int64_t T, int n_iter, const float* proj, const float* r,
                                   const float* alpha, const float* bias, float* h, void* stream) {
-    if (T < 1 || T > MHCPB_MAX_T) return MHCPB_ERR_UNSUPPORTED_SHAPE;
+    if (T < 0 || T > MHCPB_MAX_T) return MHCPB_ERR_UNSUPPORTED_SHAPE;
     const void* in[4] = {proj, r, alpha, bias};
     const size_t in_sz[4] = {(size_t)T * 32 * 4, (size_t)T * 4, 3 * 4, kNProj * 4};
     void* out[1] = {h};
     const size_t out_sz[1] = {(size_t)T * kNProj * 4};
     mhcpb_status_t s = gate_checks(T, n_iter, in, in_sz, 4, out, out_sz, 1);
-    if (s != MHCPB_OK) return s;
+    if (s != MHCPB_OK || T == 0) return s;   // no tokens: nothing to write
     cudaError_t e = gates::launch_forward(T, n_iter, proj, r, alpha, bias, h,
                                           reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MHCPB_OK : cuda_fail(e, "launch (gate forward)");
@@ -586,13 +604,13 @@ mhcpb_status_t mhcpb_gate_forward(int64_t T, int n_iter, const float* proj, cons
 mhcpb_status_t mhcpb_gate_backward(int64_t T, int n_iter, const float* proj, const float* r,
                                    const float* alpha, const float* bias, const float* grad_h,
                                    float* grad_proj, float* grad_r, float* dlogits, void* stream) {
-    if (T < 1 || T > MHCPB_MAX_T) return MHCPB_ERR_UNSUPPORTED_SHAPE;
+    if (T < 0 || T > MHCPB_MAX_T) return MHCPB_ERR_UNSUPPORTED_SHAPE;
     const void* in[5] = {proj, r, alpha, bias, grad_h};
     const size_t in_sz[5] = {(size_t)T * 32 * 4, (size_t)T * 4, 3 * 4, kNProj * 4, (size_t)T * kNProj * 4};
     void* out[3] = {grad_proj, grad_r, dlogits};
     const size_t out_sz[3] = {(size_t)T * 32 * 4, (size_t)T * 4, (size_t)T * kNProj * 4};
     mhcpb_status_t s = gate_checks(T, n_iter, in, in_sz, 5, out, out_sz, dlogits ? 3 : 2);
-    if (s != MHCPB_OK) return s;
+    if (s != MHCPB_OK || T == 0) return s;   // no tokens: nothing to write
     cudaError_t e = gates::launch_backward(T, n_iter, proj, r, alpha, bias, grad_h, grad_proj,
                                            grad_r, dlogits, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MHCPB_OK : cuda_fail(e, "launch (gate backward)");

@@ -89,21 +89,30 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
     if ((flags & ~(uint32_t)(MHCPB_ALLOW_TF32 | MHCPB_HAS_ADDEND | MHCPB_COMPENSATED_DW |
                              MHCPB_ACCUMULATE_DW)) != 0)
         return MHCPB_ERR_INVALID_ARG;
-    if (T < 1 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
+    if (T < 0 || T > MHCPB_MAX_T || K < 8 || K > MHCPB_MAX_K || (K % 8) != 0)
         return MHCPB_ERR_UNSUPPORTED_SHAPE;
     const int chunk = partial_tokens(T);
     const int64_t S = (T + chunk - 1) / chunk;
     const size_t need = (size_t)S * kNProj * (size_t)K * sizeof(float);
     if (need > kScratchBytes) return MHCPB_ERR_SCRATCH_TOO_SMALL;
     const bool add = (flags & MHCPB_HAS_ADDEND) != 0;
-    if (!x || !w || !grad_proj || !grad_r || !r || !dx || !dw) return MHCPB_ERR_INVALID_ARG;
-    if (add != (grad_x_addend != nullptr)) return MHCPB_ERR_INVALID_ARG;
+    // an operand with no elements (at T = 0: all but W and dW) needs no
+    // storage and its pointer is not checked
+    const void* all[8] = {x, w, grad_proj, grad_r, r, dx, dw, grad_x_addend};
+    const size_t all_sizes[8] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4), (size_t)(T * kGradProjCols * 4),
+                                 (size_t)(T * 4), (size_t)(T * 4), (size_t)(T * K * 2),
+                                 (size_t)(kNProj * K * 4), (size_t)(T * K * 2)};
+    const void* ptrs[8];
+    size_t sizes[8];
+    int n = 0;
+    for (int i = 0; i < (add ? 8 : 7); ++i) {
+        if (all_sizes[i] == 0) continue;
+        if (all[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
+        ptrs[n] = all[i];
+        sizes[n++] = all_sizes[i];
+    }
+    if (T > 0 && add != (grad_x_addend != nullptr)) return MHCPB_ERR_INVALID_ARG;
 
-    const void* ptrs[8] = {x, w, grad_proj, grad_r, r, dx, dw, grad_x_addend};
-    const size_t sizes[8] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4), (size_t)(T * kGradProjCols * 4),
-                             (size_t)(T * 4), (size_t)(T * 4), (size_t)(T * K * 2),
-                             (size_t)(kNProj * K * 4), (size_t)(T * K * 2)};
-    const int n = add ? 8 : 7;
     for (int i = 0; i < n; ++i)
         if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != 0) return MHCPB_ERR_MISALIGNED;
     for (int i = 0; i < n; ++i)
@@ -141,15 +150,17 @@ extern "C" mhcpb_status_t mhcpb_execute_static_scratch(int64_t T, int64_t K, uin
     p.timeout_ns = 1000000000ull;
     p.test_flags = 0;
 
-    CUtensorMap m[6];
-    if (const char* bad = encode_tc_maps(m, T, K, x, dx, add ? grad_x_addend : x, grad_proj, grad_r, r))
-        return (mhcpb_status_t)record_cuda_error(cudaErrorInvalidValue, bad);
-    const int64_t items = (int64_t)p.n_strips * p.S;
-    p.half_units = tc::use_half_units(items, s.sms) ? 1 : 0;
-    const int grid = tc::grid_size(items, s.sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], grid, st)) != cudaSuccess)
-        return (mhcpb_status_t)record_cuda_error(e, "launch (tensor-core kernel)");
+    if (T > 0) {   // T = 0: no dX, no partials; the reduction below writes dW = 0 (or dW + 0)
+        CUtensorMap m[6];
+        if (const char* bad = encode_tc_maps(m, T, K, x, dx, add ? grad_x_addend : x, grad_proj, grad_r, r))
+            return (mhcpb_status_t)record_cuda_error(cudaErrorInvalidValue, bad);
+        const int64_t items = (int64_t)p.n_strips * p.S;
+        p.half_units = tc::use_half_units(items, s.sms) ? 1 : 0;
+        const int grid = tc::grid_size(items, s.sms);
+        if ((e = tc::launch(p, m[0], m[1], m[2], m[3], m[4], m[5], grid, st)) != cudaSuccess)
+            return (mhcpb_status_t)record_cuda_error(e, "launch (tensor-core kernel)");
+    }
     if ((e = launch_reduce(p.partial, dw, p.S, (int64_t)kNProj * K,
                            (flags & MHCPB_COMPENSATED_DW) != 0,
                            (flags & MHCPB_ACCUMULATE_DW) != 0, true, st)) != cudaSuccess)

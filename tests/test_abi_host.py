@@ -57,7 +57,7 @@ def test_status_strings(lib):
     (100, 512, 0, abi.MHCPB_ERR_TF32_NOT_ALLOWED),
     (100, 512, abi.MHCPB_HAS_ADDEND, abi.MHCPB_ERR_TF32_NOT_ALLOWED),
     (100, 512, abi.MHCPB_ALLOW_TF32 | 64, abi.MHCPB_ERR_INVALID_ARG),
-    (0, 512, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
+    (-1, 512, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
     (-5, 512, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
     (100, 0, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
     (100, 12, abi.MHCPB_ALLOW_TF32, abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
@@ -69,6 +69,18 @@ def test_plan_create_rejects_before_cuda(lib, T, K, flags, status):
     with pytest.raises(abi.MhcpbError) as ei:
         abi.mhcpb_plan_create(T, K, 0, flags)
     assert ei.value.status == status
+
+
+def test_empty_batch_passes_the_shape_check(lib):
+    """T = 0 is a valid shape (an empty batch: dW = 0).  Without a GPU the
+    call then fails at the device query, not at the shape check."""
+    try:
+        h = abi.mhcpb_plan_create(0, 512, 0, abi.MHCPB_ALLOW_TF32)
+    except abi.MhcpbError as e:
+        assert e.status != abi.MHCPB_ERR_UNSUPPORTED_SHAPE
+    else:   # on a GPU machine the plan is created
+        assert abi.mhcpb_workspace_bytes(h) == 0
+        abi.mhcpb_destroy(h)
 
 
 def test_null_arguments_rejected(lib):

@@ -29,7 +29,7 @@ int main(void) {
     int64_t value = 0;
     float f = 0.f;
     EXPECT(1, mhcpb_plan_create(&plan, 100, 512, 0, 0u) == MHCPB_ERR_TF32_NOT_ALLOWED);
-    EXPECT(2, mhcpb_plan_create(&plan, 0, 512, 0, MHCPB_ALLOW_TF32) == MHCPB_ERR_UNSUPPORTED_SHAPE);
+    EXPECT(2, mhcpb_plan_create(&plan, -1, 512, 0, MHCPB_ALLOW_TF32) == MHCPB_ERR_UNSUPPORTED_SHAPE);
     EXPECT(3, mhcpb_plan_create(&plan, 100, 12, 0, MHCPB_ALLOW_TF32) == MHCPB_ERR_UNSUPPORTED_SHAPE);
     EXPECT(4, mhcpb_plan_create(&plan, (int64_t)MHCPB_MAX_T + 1, 512, 0, MHCPB_ALLOW_TF32) ==
               MHCPB_ERR_UNSUPPORTED_SHAPE);
@@ -39,7 +39,7 @@ int main(void) {
     EXPECT(8, mhcpb_plan_query(NULL, 0, &value) == MHCPB_ERR_INVALID_ARG);
     EXPECT(9, mhcpb_destroy(NULL) == MHCPB_OK);
     /* the gate calls check the shape before anything else */
-    EXPECT(10, mhcpb_gate_forward(0, 20, &f, &f, &f, &f, &f, NULL) == MHCPB_ERR_UNSUPPORTED_SHAPE);
+    EXPECT(10, mhcpb_gate_forward(-1, 20, &f, &f, &f, &f, &f, NULL) == MHCPB_ERR_UNSUPPORTED_SHAPE);
     EXPECT(11, mhcpb_gate_forward(4, MHCPB_GATE_MAX_ITER + 1, &f, &f, &f, &f, &f, NULL) ==
                MHCPB_ERR_UNSUPPORTED_SHAPE);
     EXPECT(12, strlen(mhcpb_status_string(MHCPB_OK)) > 0);

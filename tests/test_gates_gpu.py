@@ -113,7 +113,7 @@ def test_gate_rejections_write_nothing():
                                          P(d["gh"]), P(gp), P(gr), None, st), abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
         (lambda: abi.mhcpb_gate_backward(64, 65, P(d["proj"]), P(d["r"]), P(d["alpha"]), P(d["bias"]),
                                          P(d["gh"]), P(gp), P(gr), None, st), abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
-        (lambda: abi.mhcpb_gate_backward(0, 20, P(d["proj"]), P(d["r"]), P(d["alpha"]), P(d["bias"]),
+        (lambda: abi.mhcpb_gate_backward(-1, 20, P(d["proj"]), P(d["r"]), P(d["alpha"]), P(d["bias"]),
                                          P(d["gh"]), P(gp), P(gr), None, st), abi.MHCPB_ERR_UNSUPPORTED_SHAPE),
         (lambda: abi.mhcpb_gate_backward(64, 20, P(d["proj"]) + 2, P(d["r"]), P(d["alpha"]), P(d["bias"]),
                                          P(d["gh"]), P(gp), P(gr), None, st), abi.MHCPB_ERR_MISALIGNED),
