@@ -64,12 +64,12 @@ def test_edge_rows_six_decades():
 
 
 @pytest.mark.parametrize("name", ["training_profile", "long_sublayer"])
-def test_full_size_sampled_rows(name):
+def test_full_size_every_row(name):
+    """Every element of proj and r at the full sizes (the oracle works in
+    blocks of 1024 rows), with the launch configuration the bench times."""
     wl = WL.config(name)
     proj, r = run_forward(wl)
-    rng = np.random.default_rng(3)
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, wl.T - 1], rng.integers(0, wl.T, 60)]))
-    assert_forward_parity(wl, proj, r, rows=rows, label=name)
+    assert_forward_parity(wl, proj, r, label=name)
     assert np.all(proj[:, 24:] == 0)
 
 
