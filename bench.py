@@ -256,7 +256,7 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU arm
 # the sources the streaming (tensor-core) kernel is compiled from
-_STREAMING_KERNEL_SOURCES = ("mhcpb_internal.h", "mhcpb_tc.cu", "mhcpb_wait.cuh", "ptx.cuh")
+_STREAMING_KERNEL_SOURCES = ("mhcpb_check.cuh", "mhcpb_internal.h", "mhcpb_tc.cu", "mhcpb_wait.cuh", "ptx.cuh")
 
 
 def _l2_bytes(dev):

@@ -217,6 +217,18 @@ mhcpb_status_t mhcpb_get_device_status(mhcpb_plan_t plan, mhcpb_status_t* status
  * dW partial. */
 mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value);
 
+/* Bounds checks of a checked build.  A library compiled with -DMHCPB_CHECKED
+ * checks every global-memory access its kernels make at a computed address
+ * (tensor-map copies are bounded by their maps) against the extent of its
+ * buffer, skips an access found outside and records the first such site of
+ * each kernel family.  This call copies those records and clears them:
+ * sites[5] = {tensor-core backward, FMA backward, dW reduction, forward, gate
+ * kernels}, each 0 (none since the last call) or 1 + the site within that
+ * family's source.  *checked is 1 for a checked build; a normal build sets
+ * it to 0 and every site to 0, makes no CUDA call and cannot fail.  The
+ * words are per device (the current one) and shared by all plans. */
+mhcpb_status_t mhcpb_debug_checked_sites(uint32_t* sites, int* checked);
+
 /* Sets the bound on every wait inside the plan's kernels (default 1 s,
  * accepted range 1 ms .. 60 s).  A wait that runs out ends the kernel early
  * with MHCPB_ERR_DEVICE_TIMEOUT in the status word.  Applies to executes

@@ -50,7 +50,8 @@ EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcp
             "mhcpb_destroy", "mhcpb_status_string", "mhcpb_last_cuda_error",
             "mhcpb_execute_static_scratch", "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx",
             "mhcpb_reduce_dw", "mhcpb_forward_workspace_bytes", "mhcpb_forward",
-            "mhcpb_forward_profiled", "mhcpb_gate_forward", "mhcpb_gate_backward")
+            "mhcpb_forward_profiled", "mhcpb_gate_forward", "mhcpb_gate_backward",
+            "mhcpb_debug_checked_sites")
 
 
 class MhcpbError(RuntimeError):
@@ -92,6 +93,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_forward_profiled.argtypes = [P, P, P, ctypes.c_float, P, P, P, SZ, P, P, P, P]
     lib.mhcpb_gate_forward.argtypes = [I64, I32, P, P, P, P, P, P]
     lib.mhcpb_gate_backward.argtypes = [I64, I32, P, P, P, P, P, P, P, P, P]
+    lib.mhcpb_debug_checked_sites.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(I32)]
     lib.mhcpb_destroy.argtypes = [P]
     lib.mhcpb_status_string.argtypes = [I32]
     lib.mhcpb_status_string.restype = ctypes.c_char_p
@@ -102,7 +104,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch",
                  "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx", "mhcpb_reduce_dw",
                  "mhcpb_forward_workspace_bytes", "mhcpb_forward", "mhcpb_forward_profiled",
-                 "mhcpb_gate_forward", "mhcpb_gate_backward"):
+                 "mhcpb_gate_forward", "mhcpb_gate_backward", "mhcpb_debug_checked_sites"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -224,3 +226,16 @@ def mhcpb_gate_backward(T: int, n_iter: int, proj: int, r: int, alpha: int, bias
     _check(load().mhcpb_gate_backward(int(T), int(n_iter), proj, r, alpha, bias, grad_h, grad_proj,
                                       grad_r, dlogits or None, stream or None),
            "mhcpb_gate_backward")
+
+
+CHECKED_FAMILIES = ("tensor-core backward", "FMA backward", "dW reduction", "forward", "gate kernels")
+
+
+def mhcpb_debug_checked_sites():
+    """(checked, sites): whether the loaded library is a bounds-checked build,
+    and per kernel family the first out-of-range site recorded since the last
+    call (0: none; else 1 + the site), which the call clears."""
+    sites = (ctypes.c_uint32 * 5)()
+    checked = ctypes.c_int()
+    _check(load().mhcpb_debug_checked_sites(sites, ctypes.byref(checked)), "mhcpb_debug_checked_sites")
+    return bool(checked.value), dict(zip(CHECKED_FAMILIES, list(sites)))

@@ -34,6 +34,7 @@
 #include <cstdint>
 
 #include "mhcpb.h"
+#include "mhcpb_check.cuh"
 #include "mhcpb_internal.h"
 
 namespace mhcpb {
@@ -130,15 +131,19 @@ __global__ void __launch_bounds__(kThreads) gate_forward_kernel(int64_t T, int n
                                                                  const float* __restrict__ bias,
                                                                  float* __restrict__ h) {
     const Lane L = lane_of(T);
-    const float rv = L.valid ? r[L.t] : 1.f;
-    const float pres = L.valid ? proj[L.t * 32 + 8 + L.l] : 0.f;
+    // extents (bytes) for the checks of a checked build
+    const size_t t4 = (size_t)T * 4, proj_bytes = (size_t)T * 32 * 4, h_bytes = (size_t)T * kNProj * 4;
+    const float rv = L.valid && check::in(r + L.t, 4, r, t4, 0) ? r[L.t] : 1.f;
+    const float pres = L.valid && check::in(proj + L.t * 32 + 8 + L.l, 4, proj, proj_bytes, 1)
+                           ? proj[L.t * 32 + 8 + L.l] : 0.f;
     const float M = sinkhorn(alpha[2] * pres / rv + bias[8 + L.l], n_iter, nullptr, nullptr);
     if (!L.valid) return;
-    h[L.t * kNProj + 8 + L.l] = M;
+    if (check::in(h + L.t * kNProj + 8 + L.l, 4, h, h_bytes, 3)) h[L.t * kNProj + 8 + L.l] = M;
     if (L.l < 8) {
         const float a = L.l < 4 ? alpha[0] : alpha[1];
-        const float s = sigmoid(a * proj[L.t * 32 + L.l] / rv + bias[L.l]);
-        h[L.t * kNProj + L.l] = L.l < 4 ? s : 2.f * s;
+        const float pg = check::in(proj + L.t * 32 + L.l, 4, proj, proj_bytes, 1) ? proj[L.t * 32 + L.l] : 0.f;
+        const float s = sigmoid(a * pg / rv + bias[L.l]);
+        if (check::in(h + L.t * kNProj + L.l, 4, h, h_bytes, 3)) h[L.t * kNProj + L.l] = L.l < 4 ? s : 2.f * s;
     }
 }
 
@@ -153,14 +158,18 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     float* Rs = iters;
     float* Ms = iters + (size_t)n_iter * kThreads;
     const Lane L = lane_of(T);
-    const float rv = L.valid ? r[L.t] : 1.f;
+    // extents (bytes) for the checks of a checked build
+    const size_t t4 = (size_t)T * 4, proj_bytes = (size_t)T * 32 * 4, h_bytes = (size_t)T * kNProj * 4;
+    const float rv = L.valid && check::in(r + L.t, 4, r, t4, 0) ? r[L.t] : 1.f;
     const float a_res = alpha[2];
-    const float pres = L.valid ? proj[L.t * 32 + 8 + L.l] : 0.f;
+    const float pres = L.valid && check::in(proj + L.t * 32 + 8 + L.l, 4, proj, proj_bytes, 1)
+                           ? proj[L.t * 32 + 8 + L.l] : 0.f;
     const float M = sinkhorn(a_res * pres / rv + bias[8 + L.l], n_iter, Rs, Ms);
     // reverse mode on log-values, last iteration first (g = dL/dlog M):
     //   column step log M = log R - LSE_col:  g <- g - M sum_col(g)
     //   row step    log R = log A - LSE_row:  g <- g - R sum_row(g)
-    float g = (L.valid ? grad_h[L.t * kNProj + 8 + L.l] : 0.f) * M;
+    float g = (L.valid && check::in(grad_h + L.t * kNProj + 8 + L.l, 4, grad_h, h_bytes, 4)
+                   ? grad_h[L.t * kNProj + 8 + L.l] : 0.f) * M;
     for (int k = n_iter - 1; k >= 0; --k) {
         g = g - Ms[k * kThreads + threadIdx.x] * col_sum(g);
         g = g - Rs[k * kThreads + threadIdx.x] * row_sum(g);
@@ -170,10 +179,11 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     float dl_g = 0.f, a_g = 0.f, pg = 0.f;
     if (L.l < 8 && L.valid) {
         a_g = L.l < 4 ? alpha[0] : alpha[1];
-        pg = proj[L.t * 32 + L.l];
+        pg = check::in(proj + L.t * 32 + L.l, 4, proj, proj_bytes, 1) ? proj[L.t * 32 + L.l] : 0.f;
         const float s = sigmoid(a_g * pg / rv + bias[L.l]);
         const float gsc = L.l < 4 ? 1.f : 2.f;
-        dl_g = grad_h[L.t * kNProj + L.l] * gsc * s * (1.f - s);
+        const float gh = check::in(grad_h + L.t * kNProj + L.l, 4, grad_h, h_bytes, 4) ? grad_h[L.t * kNProj + L.l] : 0.f;
+        dl_g = gh * gsc * s * (1.f - s);
     }
     // grad_r = -sum_j dl_j a_j proj_j / r^2 over the token's 24 columns
     float term = dl_res * a_res * pres + dl_g * a_g * pg;
@@ -183,17 +193,22 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     term += __shfl_xor_sync(kFull, term, 8, 16);
     if (!L.valid) return;
     float* gp = grad_proj + L.t * 32;
-    gp[8 + L.l] = dl_res * a_res / rv;
-    if (L.l < 8) gp[L.l] = dl_g * a_g / rv;
-    else gp[24 + (L.l - 8)] = 0.f;   // the stored width is 32
-    if (L.l == 0) grad_r[L.t] = -term / (rv * rv);
+    if (check::in(gp + 8 + L.l, 4, grad_proj, proj_bytes, 5)) gp[8 + L.l] = dl_res * a_res / rv;
+    if (L.l < 8) {
+        if (check::in(gp + L.l, 4, grad_proj, proj_bytes, 5)) gp[L.l] = dl_g * a_g / rv;
+    } else if (check::in(gp + 24 + (L.l - 8), 4, grad_proj, proj_bytes, 5)) {
+        gp[24 + (L.l - 8)] = 0.f;   // the stored width is 32
+    }
+    if (L.l == 0 && check::in(grad_r + L.t, 4, grad_r, t4, 6)) grad_r[L.t] = -term / (rv * rv);
     if (dlogits != nullptr) {
-        dlogits[L.t * kNProj + 8 + L.l] = dl_res;
-        if (L.l < 8) dlogits[L.t * kNProj + L.l] = dl_g;
+        if (check::in(dlogits + L.t * kNProj + 8 + L.l, 4, dlogits, h_bytes, 7)) dlogits[L.t * kNProj + 8 + L.l] = dl_res;
+        if (L.l < 8 && check::in(dlogits + L.t * kNProj + L.l, 4, dlogits, h_bytes, 7)) dlogits[L.t * kNProj + L.l] = dl_g;
     }
 }
 
 }  // namespace
+
+cudaError_t checked_site(uint32_t* site) { return check::read_and_clear(site); }
 
 size_t backward_smem_bytes(int n_iter) { return (size_t)(2 * n_iter) * kThreads * sizeof(float); }
 

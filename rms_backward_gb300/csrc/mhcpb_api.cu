@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "mhcpb.h"
+#include "mhcpb_check.cuh"
 #include "mhcpb_internal.h"
 
 using namespace mhcpb;
@@ -656,6 +657,17 @@ mhcpb_status_t mhcpb_destroy(mhcpb_plan_t plan) {
         if (plan->d_trace) cudaFree(plan->d_trace);
     }
     delete plan;
+    return MHCPB_OK;
+}
+
+mhcpb_status_t mhcpb_debug_checked_sites(uint32_t* sites, int* checked) {
+    if (sites == nullptr || checked == nullptr) return MHCPB_ERR_INVALID_ARG;
+    *checked = check::kEnabled ? 1 : 0;
+    cudaError_t e;
+    if ((e = tc::checked_site(&sites[0])) != cudaSuccess || (e = fma::checked_site(&sites[1])) != cudaSuccess ||
+        (e = reduce_checked_site(&sites[2])) != cudaSuccess || (e = fwd::checked_site(&sites[3])) != cudaSuccess ||
+        (e = gates::checked_site(&sites[4])) != cudaSuccess)
+        return cuda_fail(e, "checked-build site words");
     return MHCPB_OK;
 }
 

@@ -12,6 +12,7 @@
 // tensor-core kernel: the same arithmetic on the CUDA cores.
 #include <cuda_bf16.h>
 
+#include "mhcpb_check.cuh"
 #include "mhcpb_internal.h"
 #include "ptx.cuh"
 
@@ -27,6 +28,12 @@ __device__ __forceinline__ float tf32_rna(float v) {
     uint32_t u;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(v));
     return __uint_as_float(u & 0xFFFFE000u);
+}
+
+// a read-only global load, bounds-checked in checked builds (0 when outside)
+template <class V>
+__device__ __forceinline__ V ld_checked(const V* ptr, const void* base, size_t bytes, uint32_t site) {
+    return check::in(ptr, sizeof(V), base, bytes, site) ? __ldg(ptr) : V(0);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -46,13 +53,19 @@ __global__ void __launch_bounds__(kThreads) main_fma_kernel(const MainParams p) 
     const int t0 = chunk * p.chunk;
     const int nt = min(p.T - t0, p.chunk);
     const int K = p.K;
+    // buffer extents (bytes) for the checks of a checked build
+    const size_t tk_bytes = (size_t)p.T * K * 2, w_bytes = (size_t)kNProj * K * 4,
+                 gp_bytes = (size_t)p.T * kGradProjCols * 4, t_bytes = (size_t)p.T * 4,
+                 part_bytes = (size_t)p.S * kNProj * K * 4;
 
     for (int i = threadIdx.x; i < nt * kNProj; i += kThreads) {
         const int tt = i / kNProj, j = i - tt * kNProj;
-        sP[i] = tf32_rna(__ldg(p.grad_proj + (size_t)(t0 + tt) * kGradProjCols + j));
+        sP[i] = tf32_rna(ld_checked(p.grad_proj + (size_t)(t0 + tt) * kGradProjCols + j, p.grad_proj,
+                                    gp_bytes, 0));
     }
     for (int i = threadIdx.x; i < nt; i += kThreads)
-        sC[i] = __ldg(p.grad_r + t0 + i) / (__ldg(p.r + t0 + i) * static_cast<float>(K));
+        sC[i] = ld_checked(p.grad_r + t0 + i, p.grad_r, t_bytes, 1) /
+                (ld_checked(p.r + t0 + i, p.r, t_bytes, 2) * static_cast<float>(K));
     __syncthreads();
 
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -62,8 +75,8 @@ __global__ void __launch_bounds__(kThreads) main_fma_kernel(const MainParams p) 
     float w0[kNProj], w1[kNProj], a0[kNProj], a1[kNProj];
 #pragma unroll
     for (int j = 0; j < kNProj; ++j) {
-        w0[j] = valid ? tf32_rna(__ldg(p.w + (size_t)j * K + col)) : 0.f;
-        w1[j] = valid ? tf32_rna(__ldg(p.w + (size_t)j * K + col + 1)) : 0.f;
+        w0[j] = valid ? tf32_rna(ld_checked(p.w + (size_t)j * K + col, p.w, w_bytes, 3)) : 0.f;
+        w1[j] = valid ? tf32_rna(ld_checked(p.w + (size_t)j * K + col + 1, p.w, w_bytes, 3)) : 0.f;
         a0[j] = 0.f;
         a1[j] = 0.f;
     }
@@ -71,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) main_fma_kernel(const MainParams p) 
     if (valid) {
         for (int tt = ty; tt < nt; tt += kGroups) {
             const size_t off = (size_t)(t0 + tt) * K + col;
-            const uint32_t xv = __ldg(reinterpret_cast<const uint32_t*>(p.x + off));
+            const uint32_t xv = ld_checked(reinterpret_cast<const uint32_t*>(p.x + off), p.x, tk_bytes, 4);
             const float x0 = __uint_as_float(xv << 16);
             const float x1 = __uint_as_float(xv & 0xFFFF0000u);
             const float* pr = sP + tt * kNProj;
@@ -90,13 +103,14 @@ __global__ void __launch_bounds__(kThreads) main_fma_kernel(const MainParams p) 
             uint32_t out = pack_bf16x2(d0, d1);
             if (p.addend != nullptr) {
                 // the value a separate BF16 add gives: bf16(fp32(bf16 core) + fp32(addend))
-                const uint32_t av = __ldg(reinterpret_cast<const uint32_t*>(p.addend + off));
+                const uint32_t av =
+                    ld_checked(reinterpret_cast<const uint32_t*>(p.addend + off), p.addend, tk_bytes, 5);
                 const float s0 = __uint_as_float(out << 16) + __uint_as_float(av << 16);
                 const float s1 =
                     __uint_as_float(out & 0xFFFF0000u) + __uint_as_float(av & 0xFFFF0000u);
                 out = pack_bf16x2(s0, s1);
             }
-            *reinterpret_cast<uint32_t*>(p.dx + off) = out;
+            if (check::in(p.dx + off, 4, p.dx, tk_bytes, 6)) *reinterpret_cast<uint32_t*>(p.dx + off) = out;
         }
     }
     __syncthreads();   // sP is reused below
@@ -115,7 +129,8 @@ __global__ void __launch_bounds__(kThreads) main_fma_kernel(const MainParams p) 
 #pragma unroll
         for (int g = 1; g < kGroups; ++g) s += sR[(g * kNProj + j) * kStrip + cc];
         const int c2 = strip * kStrip + cc;
-        if (c2 < K) p.partial[((size_t)chunk * kNProj + j) * K + c2] = s;
+        float* dst = p.partial + ((size_t)chunk * kNProj + j) * K + c2;
+        if (c2 < K && check::in(dst, 4, p.partial, part_bytes, 7)) *dst = s;
     }
 }
 
@@ -132,6 +147,8 @@ cudaError_t setup() {
     return cudaFuncSetAttribute(main_fma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)smem_bytes());
 }
+
+cudaError_t checked_site(uint32_t* site) { return check::read_and_clear(site); }
 
 cudaError_t launch(const MainParams& p, cudaStream_t stream) {
     dim3 grid(p.n_strips, p.S);

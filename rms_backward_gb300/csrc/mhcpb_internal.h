@@ -65,6 +65,8 @@ inline int grid_size(int64_t items, int sms) {
 }
 size_t smem_bytes(bool has_addend);
 cudaError_t setup(bool has_addend);
+// checked builds: this unit's first out-of-range site (0: none), then cleared
+cudaError_t checked_site(uint32_t* site);
 // Tensor maps: x/dx/addend BF16 [T,K] boxes 64 x {128,32,128} (128-byte swizzle),
 // grad_proj FP32 [T,32] box 24 x 128, grad_r and r FP32 [T] boxes of 128.
 cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensorMap& dx_map,
@@ -79,6 +81,7 @@ constexpr int kThreads = 256;
 size_t smem_bytes();
 cudaError_t setup();
 cudaError_t launch(const MainParams& p, cudaStream_t stream);
+cudaError_t checked_site(uint32_t* site);
 }  // namespace fma
 
 // Forward of the stage (proj = X W^T over TF32 W, r = RMS of each row):
@@ -115,6 +118,7 @@ inline int grid_size(int64_t T, int64_t K, int sms) {
 }
 size_t smem_bytes();
 cudaError_t setup();
+cudaError_t checked_site(uint32_t* site);
 // launches both kernels on `stream`; x_map: X [T, K] BF16, boxes 64 x 128, 128-byte swizzle;
 // w_map: W [24, K] FP32, boxes 64 x 24, no swizzle; non-null events are
 // recorded before, between and after the two kernels
@@ -130,6 +134,7 @@ namespace gates {
 constexpr int kMaxIter = 64;
 size_t backward_smem_bytes(int n_iter);
 cudaError_t setup();
+cudaError_t checked_site(uint32_t* site);
 cudaError_t launch_forward(int64_t T, int n_iter, const float* proj, const float* r,
                            const float* alpha, const float* bias, float* h, cudaStream_t stream);
 cudaError_t launch_backward(int64_t T, int n_iter, const float* proj, const float* r,
@@ -151,6 +156,7 @@ int record_cuda_error(cudaError_t e, const char* what);
 // `accumulate`, the result is added to dW's previous contents.
 // `discard`: drop the partials' L2 lines after reading them (their contents
 // are then undefined), only where nothing reads them again.
+cudaError_t reduce_checked_site(uint32_t* site);
 cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, bool compensated,
                           bool accumulate, bool discard, cudaStream_t stream);
 

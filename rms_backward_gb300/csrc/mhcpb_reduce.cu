@@ -26,6 +26,7 @@
 // read: with a 128-byte-aligned workspace their L2 lines are dropped without
 // being written back to HBM.  A stand-alone reduction (the split call) keeps
 // them, so it can be repeated on the same workspace.
+#include "mhcpb_check.cuh"
 #include "mhcpb_internal.h"
 #include "ptx.cuh"
 
@@ -64,7 +65,8 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
         float4 b[kGroup];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
-            if (s0 + g < S) b[g] = part[(int64_t)(s0 + g) * n4 + i];
+            if (s0 + g < S && check::in(part + (int64_t)(s0 + g) * n4 + i, 16, part, (size_t)S * n4 * 16, 0))
+                b[g] = part[(int64_t)(s0 + g) * n4 + i];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g) {
             if (s0 + g < S) {
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
     if (COMP) {
         a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
     }
-    if (valid) {
+    if (valid && check::in(dw + i, 16, dw, (size_t)n4 * 16, 1)) {
         if (ACC) {   // accumulate into the caller's dW: one more FP32 rounding
             const float4 o = dw[i];
             a.x = o.x + a.x; a.y = o.y + a.y; a.z = o.z + a.z; a.w = o.w + a.w;
@@ -101,12 +103,15 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_dw_kernel(const float4*
         const int64_t w0 = i - lane;   // the warp's first float4
         for (int q = lane; q < 4 * S; q += 32) {
             const int64_t f4 = w0 + 8 * (q & 3);
-            if (f4 < n4) ptx::discard_l2_line(part + (int64_t)(q >> 2) * n4 + f4);
+            if (f4 < n4 && check::in(part + (int64_t)(q >> 2) * n4 + f4, 128, part, (size_t)S * n4 * 16, 2))
+                ptx::discard_l2_line(part + (int64_t)(q >> 2) * n4 + f4);
         }
     }
 }
 
 }  // namespace
+
+cudaError_t reduce_checked_site(uint32_t* site) { return check::read_and_clear(site); }
 
 cudaError_t launch_reduce(const float* partial, float* dw, int S, int64_t n, bool compensated,
                           bool accumulate, bool discard_allowed, cudaStream_t stream) {

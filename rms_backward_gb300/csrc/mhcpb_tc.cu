@@ -38,6 +38,7 @@
 //    records a status word, drains its own copies and MMAs and exits.
 #include <cuda_bf16.h>
 
+#include "mhcpb_check.cuh"
 #include "mhcpb_internal.h"
 #include "mhcpb_wait.cuh"
 #include "ptx.cuh"
@@ -486,7 +487,9 @@ __global__ void __launch_bounds__(Cfg<ADD>::threads, 1)
                 const int col = col0 + pw * 64 + lane + 32 * q;
 #pragma unroll
                 for (int j = 0; j < kNProj; ++j)
-                    wv[q][j] = col < p.K ? __ldg(p.w + (size_t)j * p.K + col) : 0.f;
+                    wv[q][j] = col < p.K && check::in(p.w + (size_t)j * p.K + col, 4, p.w, (size_t)kNProj * p.K * 4, 0)
+                                   ? __ldg(p.w + (size_t)j * p.K + col)
+                                   : 0.f;
             }
         };
         fetch_w(item_at(p, it_begin, u_begin, u_end).col0);
@@ -594,18 +597,21 @@ __global__ void __launch_bounds__(Cfg<ADD>::threads, 1)
                 if (e == 0 && lane == 0) TRACE(EV_DRAIN_START, local);
                 const int col = I.col0 + q * 32 + lane;
                 if (col < p.K) {
+                    const size_t part_bytes = (size_t)p.S * kNProj * p.K * 4;   // checked builds
                     float* dst = p.partial + (size_t)I.chunk * kNProj * p.K + col;
                     // accumulator columns: 0-15 X^T Ph[0..15], 16-31 X^T Pl[0..15],
                     //                      32-39 X^T Ph[16..23], 40-47 X^T Pl[16..23]
                     if (lo_part) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            ptx::st_global_hint(dst + (size_t)j * p.K, __uint_as_float(d0[j]) + __uint_as_float(d1[j]), pol_keep);
+                            if (check::in(dst + (size_t)j * p.K, 4, p.partial, part_bytes, 1))
+                                ptx::st_global_hint(dst + (size_t)j * p.K, __uint_as_float(d0[j]) + __uint_as_float(d1[j]), pol_keep);
                     }
                     if (hi_part) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            ptx::st_global_hint(dst + (size_t)(16 + i) * p.K, __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]), pol_keep);
+                            if (check::in(dst + (size_t)(16 + i) * p.K, 4, p.partial, part_bytes, 1))
+                                ptx::st_global_hint(dst + (size_t)(16 + i) * p.K, __uint_as_float(d2[i]) + __uint_as_float(d2[8 + i]), pol_keep);
                     }
                 }
                 if (e == 0 && lane == 0) TRACE(EV_DRAIN_END, local);
@@ -769,6 +775,8 @@ cudaError_t launch_one(const MainParams& p, const Maps& m, int grid, cudaStream_
 size_t smem_bytes(bool has_addend) { return has_addend ? Cfg<true>::alloc : Cfg<false>::alloc; }
 
 cudaError_t setup(bool has_addend) { return has_addend ? setup_one<true>() : setup_one<false>(); }
+
+cudaError_t checked_site(uint32_t* site) { return check::read_and_clear(site); }
 
 cudaError_t launch(const MainParams& p, const CUtensorMap& x_map, const CUtensorMap& dx_map,
                    const CUtensorMap& add_map, const CUtensorMap& gp_map, const CUtensorMap& gr_map,

@@ -43,6 +43,7 @@
 // partial lines from L2.  Every mbarrier wait is bounded (wait_bar).
 #include <cuda_bf16.h>
 
+#include "mhcpb_check.cuh"
 #include "mhcpb_internal.h"
 #include "mhcpb_wait.cuh"
 #include "ptx.cuh"
@@ -420,12 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // partial[fc][j][t] (token-contiguous rows: a warp writes 128 bytes per j)
                 float* dst = p.partial + (size_t)U.fc * kPartRows * p.t_pad + t;
 #pragma unroll
+                const size_t part_bytes = (size_t)p.n_fc * kPartRows * p.t_pad * 4;   // checked builds
                 for (int j = 0; j < kNProj; ++j) {
                     const float hi = __uint_as_float(j < 16 ? d0[j] : d1[j - 16]);
                     const float lo = __uint_as_float(j < 8 ? d1[8 + j] : d2[j - 8]);
-                    ptx::st_global_hint(dst + (size_t)j * p.t_pad, hi + lo, pol_keep);
+                    if (check::in(dst + (size_t)j * p.t_pad, 4, p.partial, part_bytes, 0))
+                        ptx::st_global_hint(dst + (size_t)j * p.t_pad, hi + lo, pol_keep);
                 }
-                ptx::st_global_hint(dst + (size_t)kNProj * p.t_pad, ss, pol_keep);
+                if (check::in(dst + (size_t)kNProj * p.t_pad, 4, p.partial, part_bytes, 0))
+                    ptx::st_global_hint(dst + (size_t)kNProj * p.t_pad, ss, pol_keep);
             }
             if (q == 0 && lane == 0) FTRACE(F_DRAIN_END, un);
             if (++ab == 2) { ab = 0; aph ^= 1u; }
@@ -461,13 +465,14 @@ constexpr int kOutThreads = 256;
 
 // the ascending-order sum over the chunks of one partial element (src points
 // at chunk 0; stride floats per chunk), every group's loads in flight together
-__device__ __forceinline__ float sum_chunks(const float* src, int64_t stride, int n_fc) {
+__device__ __forceinline__ float sum_chunks(const float* src, int64_t stride, int n_fc, const float* part) {
     float a = 0.f;
     for (int f0 = 0; f0 < n_fc; f0 += kGroup) {
         float b[kGroup];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
-            if (f0 + g < n_fc) b[g] = src[(int64_t)(f0 + g) * stride];
+            if (f0 + g < n_fc && check::in(src + (int64_t)(f0 + g) * stride, 4, part, (size_t)n_fc * stride * 4, 1))
+                b[g] = src[(int64_t)(f0 + g) * stride];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
             if (f0 + g < n_fc) a = (f0 + g == 0) ? b[g] : a + b[g];
@@ -486,12 +491,14 @@ __global__ void __launch_bounds__(kLineThreads)
     const int t0 = blockIdx.x * kLineTokens;   // gridDim.x = t_pad / 32: t0 + lane < t_pad
     const int64_t stride = (int64_t)kPartRows * t_pad;   // floats per chunk
     const float* src = part + (int64_t)row * t_pad + t0;
-    sums[row][lane] = sum_chunks(src + lane, stride, n_fc);
+    sums[row][lane] = sum_chunks(src + lane, stride, n_fc, part);
     // the partials are dead once read: drop the warp's line of every chunk
     // from L2, spread over the lanes
     __syncwarp();
     if (discard)
-        for (int f = lane; f < n_fc; f += 32) ptx::discard_l2_line(src + (int64_t)f * stride);
+        for (int f = lane; f < n_fc; f += 32)
+            if (check::in(src + (int64_t)f * stride, 128, part, (size_t)n_fc * stride * 4, 4))
+                ptx::discard_l2_line(src + (int64_t)f * stride);
     __syncthreads();
     if (threadIdx.x < kLineTokens * kProjCols / 4) {
         // 32 proj rows x 8 float4: columns 24..31 are the zero pad
@@ -503,12 +510,14 @@ __global__ void __launch_bounds__(kLineThreads)
             v.y = c + 1 < kNProj ? sums[c + 1][tt] : 0.f;
             v.z = c + 2 < kNProj ? sums[c + 2][tt] : 0.f;
             v.w = c + 3 < kNProj ? sums[c + 3][tt] : 0.f;
-            *reinterpret_cast<float4*>(proj + (size_t)t * kProjCols + c) = v;
+            if (check::in(proj + (size_t)t * kProjCols + c, 16, proj, (size_t)T * kProjCols * 4, 2))
+                *reinterpret_cast<float4*>(proj + (size_t)t * kProjCols + c) = v;
         }
     } else if (threadIdx.x < kLineTokens * kProjCols / 4 + kLineTokens) {
         const int tt = threadIdx.x - kLineTokens * kProjCols / 4;
         const int t = t0 + tt;
-        if (t < T) r[t] = sqrtf(sums[kNProj][tt] / kf + eps);   // the mean of the squares, eps, root
+        if (t < T && check::in(r + t, 4, r, (size_t)T * 4, 3))
+            r[t] = sqrtf(sums[kNProj][tt] / kf + eps);   // the mean of the squares, eps, root
     }
 }
 
@@ -524,28 +533,36 @@ __global__ void __launch_bounds__(kOutThreads)
     const int t = valid ? (int)(i - (int64_t)row * t_pad) : 0;
     const int64_t stride = (int64_t)kPartRows * t_pad;
     const int64_t base = (int64_t)row * t_pad + t;
-    const float a = valid ? sum_chunks(part + base, stride, n_fc) : 0.f;
+    const float a = valid ? sum_chunks(part + base, stride, n_fc, part) : 0.f;
     if (valid && t < T) {
+        const size_t proj_bytes = (size_t)T * kProjCols * 4;   // checked builds
         if (row < kNProj) {
-            proj[(size_t)t * kProjCols + row] = a;
+            if (check::in(proj + (size_t)t * kProjCols + row, 4, proj, proj_bytes, 2))
+                proj[(size_t)t * kProjCols + row] = a;
         } else {
-            r[t] = sqrtf(a / kf + eps);
+            if (check::in(r + t, 4, r, (size_t)T * 4, 3)) r[t] = sqrtf(a / kf + eps);
             float4* pad = reinterpret_cast<float4*>(proj + (size_t)t * kProjCols + kNProj);
-            pad[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            pad[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (check::in(pad, 32, proj, proj_bytes, 2)) {
+                pad[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                pad[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
     }
     // the warp's line of each chunk (32 tokens of one row), spread over the lanes
     __syncwarp();
     if (valid && discard) {
         const int64_t b0 = base - (t & 31);
-        for (int f = t & 31; f < n_fc; f += 32) ptx::discard_l2_line(part + (int64_t)f * stride + b0);
+        for (int f = t & 31; f < n_fc; f += 32)
+            if (check::in(part + (int64_t)f * stride + b0, 128, part, (size_t)n_fc * stride * 4, 4))
+                ptx::discard_l2_line(part + (int64_t)f * stride + b0);
     }
 }
 
 }  // namespace
 
 size_t smem_bytes() { return kSmem; }
+
+cudaError_t checked_site(uint32_t* site) { return check::read_and_clear(site); }
 
 cudaError_t setup() {
     return cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
