@@ -396,6 +396,31 @@ def _forward_side(plan, x, w, flush, stream, T, K, peak, reps=100):
         k2.append(e1.elapsed_time(e2))
     if plan.device_status() != 0:
         raise RuntimeError("device-side timeout in the forward")
+    # the gate step after it: fused into the forward's reduction, and as the
+    # separate gate call after the plain forward (flushed before each pair)
+    rng = np.random.default_rng(0)
+    alpha = torch.from_numpy(rng.uniform(0.5, 1.5, 3).astype(np.float32)).to(x.device)
+    bias = torch.from_numpy(rng.normal(0, 0.5, 24).astype(np.float32)).to(x.device)
+    h = torch.empty((T, 24), dtype=torch.float32, device=x.device)
+    from rms_backward_gb300 import mhc_gate_forward
+
+    def fused():
+        abi.mhcpb_forward_gates(plan.handle, x.data_ptr(), w.data_ptr(), eps, alpha.data_ptr(),
+                                bias.data_ptr(), 20, proj.data_ptr(), r.data_ptr(), h.data_ptr(),
+                                ws.data_ptr(), wsb, sh)
+
+    def separate():
+        call()
+        mhc_gate_forward(proj, r, alpha, bias, h, n_iter=20, stream=sh)
+
+    for _ in range(3):
+        flush.fill_(1.0)
+        fused()
+        separate()
+    t_fused = _step_times(fused, flush, reps, "flushed", stream)
+    t_sep = _step_times(separate, flush, reps, "flushed", stream)
+    if plan.device_status() != 0:
+        raise RuntimeError("device-side timeout in the forward")
     alg = WL.algorithmic_bytes_forward(T, K)
     med = float(np.median(times))
     k1_bytes = 2 * T * K + 96 * K
@@ -407,7 +432,11 @@ def _forward_side(plan, x, w, flush, stream, T, K, peak, reps=100):
             "kernel_us": k1_mean * 1e3, "kernel_median_us": float(np.median(k1)) * 1e3,
             "reduce_us": float(np.mean(k2)) * 1e3,
             "kernel_frac": k1_bytes / (k1_mean * 1e-3) / 1e9 / peak,
-            "kernel_algorithmic_bytes": k1_bytes}
+            "kernel_algorithmic_bytes": k1_bytes,
+            "with_gates": {"fused_flushed": _stats_us(t_fused), "separate_flushed": _stats_us(t_sep),
+                           "n_iter": 20,
+                           "how": "mhcpb_forward_gates against mhcpb_forward then mhcpb_gate_forward, "
+                                  "L2 flushed before each call or pair; median of the per-call times"}}
 
 
 def _gates_side(T, flush, stream, peak, reps=100, n_iter=20):

@@ -324,6 +324,21 @@ mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const fl
                                       size_t workspace_bytes, void* stream, void* ev_before,
                                       void* ev_between, void* ev_after);
 
+/* The forward with the gate step fused into its second kernel (the
+ * prime-kernels PR #15 page's mhc_projection fuses the gate activations,
+ * sigmoid and Sinkhorn, into the projection): writes proj and r exactly as
+ * mhcpb_forward does, and h [T, 24] from them exactly as mhcpb_gate_forward
+ * (below) would from the stored proj and r with the same alpha, bias and
+ * n_iter: the same bits, one kernel launch fewer.  alpha [3], bias [24] and
+ * h follow mhcpb_gate_forward's rules (device memory of the plan's device,
+ * 4-byte aligned; h overlaps no other operand), the rest mhcpb_forward's.
+ * n_iter outside 1 .. MHCPB_GATE_MAX_ITER: MHCPB_ERR_UNSUPPORTED_SHAPE.  The
+ * reduction always takes its line layout here. */
+mhcpb_status_t mhcpb_forward_gates(mhcpb_plan_t plan, const void* x, const float* w, float eps,
+                                   const float* alpha, const float* bias, int n_iter, float* proj,
+                                   float* r, float* h, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
 /* ---------------------------------------------------------------------------
  * The gate/normalisation step around the stage: the forward turns the
  * projection logits and r into the mHC gates; the backward turns the gates'

@@ -97,6 +97,16 @@ class Plan:
                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                       self._stream(stream, x))
 
+    def forward_gates(self, x, w, alpha, bias, proj, r, h, workspace, eps: float = 1e-6,
+                      n_iter: int = 20, stream=None):
+        """The forward with the gate step fused in: proj and r as ``forward``,
+        and h [T, 24] as ``mhc_gate_forward`` gives from them (see
+        ``mhcpb_forward_gates``)."""
+        abi.mhcpb_forward_gates(self.handle, x.data_ptr(), w.data_ptr(), eps, alpha.data_ptr(),
+                                bias.data_ptr(), n_iter, proj.data_ptr(), r.data_ptr(), h.data_ptr(),
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                self._stream(stream, x))
+
     def device_status(self, clear: bool = False) -> int:
         return mhcpb_get_device_status(self.handle, clear)
 

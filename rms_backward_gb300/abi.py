@@ -51,7 +51,7 @@ EXPORTED = ("mhcpb_plan_create", "mhcpb_workspace_bytes", "mhcpb_execute", "mhcp
             "mhcpb_execute_static_scratch", "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx",
             "mhcpb_reduce_dw", "mhcpb_forward_workspace_bytes", "mhcpb_forward",
             "mhcpb_forward_profiled", "mhcpb_gate_forward", "mhcpb_gate_backward",
-            "mhcpb_debug_checked_sites")
+            "mhcpb_debug_checked_sites", "mhcpb_forward_gates")
 
 
 class MhcpbError(RuntimeError):
@@ -91,6 +91,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mhcpb_forward_workspace_bytes.argtypes = [P, ctypes.POINTER(SZ)]
     lib.mhcpb_forward.argtypes = [P, P, P, ctypes.c_float, P, P, P, SZ, P]
     lib.mhcpb_forward_profiled.argtypes = [P, P, P, ctypes.c_float, P, P, P, SZ, P, P, P, P]
+    lib.mhcpb_forward_gates.argtypes = [P, P, P, ctypes.c_float, P, P, I32, P, P, P, P, SZ, P]
     lib.mhcpb_gate_forward.argtypes = [I64, I32, P, P, P, P, P, P]
     lib.mhcpb_gate_backward.argtypes = [I64, I32, P, P, P, P, P, P, P, P, P]
     lib.mhcpb_debug_checked_sites.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(I32)]
@@ -104,7 +105,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "mhcpb_plan_set_wait_limit", "mhcpb_destroy", "mhcpb_execute_static_scratch",
                  "mhcpb_plan_set_max_ctas", "mhcpb_execute_dx", "mhcpb_reduce_dw",
                  "mhcpb_forward_workspace_bytes", "mhcpb_forward", "mhcpb_forward_profiled",
-                 "mhcpb_gate_forward", "mhcpb_gate_backward", "mhcpb_debug_checked_sites"):
+                 "mhcpb_gate_forward", "mhcpb_gate_backward", "mhcpb_debug_checked_sites",
+                 "mhcpb_forward_gates"):
         getattr(lib, name).restype = I32
     _lib = lib
     return lib
@@ -165,6 +167,15 @@ def mhcpb_forward(plan: int, x: int, w: int, eps: float, proj: int, r: int, work
                   workspace_bytes: int, stream: int | None) -> None:
     _check(load().mhcpb_forward(plan, x, w, float(eps), proj, r, workspace, int(workspace_bytes),
                                 stream or None), "mhcpb_forward")
+
+
+def mhcpb_forward_gates(plan: int, x: int, w: int, eps: float, alpha: int, bias: int, n_iter: int,
+                        proj: int, r: int, h: int, workspace: int, workspace_bytes: int,
+                        stream: int | None) -> None:
+    """The forward with the gate step fused into its reduction: proj, r and h."""
+    _check(load().mhcpb_forward_gates(plan, x, w, float(eps), alpha, bias, int(n_iter), proj, r, h,
+                                      workspace, int(workspace_bytes), stream or None),
+           "mhcpb_forward_gates")
 
 
 def mhcpb_get_device_status(plan: int, clear: bool = False) -> int:

@@ -17,14 +17,9 @@
 // (and lane g < 8 also pre/post gate g), so every row sum is a 2-step and every
 // column sum a 2-step shuffle inside the half-warp.  FP32 throughout.
 //
-// The iterations first run directly on exp(l - row maximum), dividing by sums
-// through their correctly rounded reciprocals.  Where a token's sums leave
-// the normal FP32 range (logits ~90 or more apart leave a whole column at 0,
-// or the inputs hold NaN), the warp redoes its tokens on logarithms: a row
-// normalisation is log R = log A - LSE_row(log A), a column normalisation
-// log M = log R - LSE_col(log R), each log-sum-exp taken after subtracting the
-// maximum, so no sum can underflow.  Both give the same R and M up to
-// rounding.  The backward carries the gradient with respect to the logarithms: through
+// The per-token arithmetic (Sinkhorn iterations, direct with a log-domain
+// fallback, and the gates) is in mhcg_math.cuh, shared with the forward's
+// fused reduction.  The backward carries the gradient with respect to the logarithms: through
 // a column step g <- g - M colsum(g), through a row step g <- g - R rowsum(g),
 // starting from G_res * M and ending at dL/dl_res -- the chain rule of the
 // normalisations written for log-values, with no division.  It keeps R and M
@@ -33,6 +28,7 @@
 
 #include <cstdint>
 
+#include "mhcg_math.cuh"
 #include "mhcpb.h"
 #include "mhcpb_check.cuh"
 #include "mhcpb_internal.h"
@@ -44,24 +40,9 @@ namespace {
 
 constexpr int kThreads = 256;            // 16 tokens per block
 constexpr int kTokensPerBlock = kThreads / 16;
-constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ float row_sum(float v) {   // lanes 4i .. 4i+3 of the half-warp
-    v += __shfl_xor_sync(kFull, v, 1, 16);
-    v += __shfl_xor_sync(kFull, v, 2, 16);
-    return v;
-}
-__device__ __forceinline__ float col_sum(float v) {   // lanes j, j+4, j+8, j+12
-    v += __shfl_xor_sync(kFull, v, 4, 16);
-    v += __shfl_xor_sync(kFull, v, 8, 16);
-    return v;
-}
-__device__ __forceinline__ float row_max(float v) {
-    v = fmaxf(v, __shfl_xor_sync(kFull, v, 1, 16));
-    v = fmaxf(v, __shfl_xor_sync(kFull, v, 2, 16));
-    return v;
-}
-__device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
+using gatemath::col_sum;
+using gatemath::kFull;
+using gatemath::row_sum;
 
 struct Lane {
     int64_t t;       // token
@@ -76,54 +57,6 @@ __device__ __forceinline__ Lane lane_of(int64_t T) {
     return L;
 }
 
-__device__ __forceinline__ float col_max(float v) {
-    v = fmaxf(v, __shfl_xor_sync(kFull, v, 4, 16));
-    v = fmaxf(v, __shfl_xor_sync(kFull, v, 8, 16));
-    return v;
-}
-// one Sinkhorn iteration on this lane's log-value: returns log M, and log R
-// (after the row step) through `lr`
-__device__ __forceinline__ float sinkhorn_step_log(float la, float& lr) {
-    const float m = row_max(la);
-    lr = la - (m + logf(row_sum(expf(la - m))));
-    const float m2 = col_max(lr);
-    return lr - (m2 + logf(col_sum(expf(lr - m2))));
-}
-// a sum the direct iterations can divide by: finite and normal with margin
-__device__ __forceinline__ bool sum_ok(float v) { return v >= 1e-30f && v <= 1e30f; }
-
-// n_iter Sinkhorn iterations of this lane's residual logit l; stores R and M
-// of every iteration when `Rs`/`Ms` are given (stride kThreads); returns the
-// final M.  Warp-uniform: every lane of the warp calls it.
-__device__ __forceinline__ float sinkhorn(float l, int n_iter, float* Rs, float* Ms) {
-    // direct: A = exp(l - row max) in (0, 1]
-    float A = expf(l - row_max(l));
-    bool ok = true;
-    for (int k = 0; k < n_iter; ++k) {
-        const float s = row_sum(A);
-        const float R = A * __frcp_rn(s);
-        const float c = col_sum(R);
-        A = R * __frcp_rn(c);
-        ok = ok && sum_ok(s) && sum_ok(c);
-        if (Rs != nullptr) {
-            Rs[k * kThreads + threadIdx.x] = R;
-            Ms[k * kThreads + threadIdx.x] = A;
-        }
-    }
-    if (!__any_sync(kFull, !ok)) return A;
-    // a sum left the safe range somewhere in this warp: redo on logarithms
-    float la = l;
-    for (int k = 0; k < n_iter; ++k) {
-        float lr;
-        la = sinkhorn_step_log(la, lr);
-        if (Rs != nullptr) {
-            Rs[k * kThreads + threadIdx.x] = expf(lr);
-            Ms[k * kThreads + threadIdx.x] = expf(la);
-        }
-    }
-    return expf(la);
-}
-
 __global__ void __launch_bounds__(kThreads) gate_forward_kernel(int64_t T, int n_iter,
                                                                  const float* __restrict__ proj,
                                                                  const float* __restrict__ r,
@@ -136,14 +69,14 @@ __global__ void __launch_bounds__(kThreads) gate_forward_kernel(int64_t T, int n
     const float rv = L.valid && check::in(r + L.t, 4, r, t4, 0) ? r[L.t] : 1.f;
     const float pres = L.valid && check::in(proj + L.t * 32 + 8 + L.l, 4, proj, proj_bytes, 1)
                            ? proj[L.t * 32 + 8 + L.l] : 0.f;
-    const float M = sinkhorn(alpha[2] * pres / rv + bias[8 + L.l], n_iter, nullptr, nullptr);
+    const float M = gatemath::sinkhorn(gatemath::res_logit(pres, rv, alpha, bias, L.l), n_iter, nullptr,
+                                       nullptr, 0);
     if (!L.valid) return;
     if (check::in(h + L.t * kNProj + 8 + L.l, 4, h, h_bytes, 3)) h[L.t * kNProj + 8 + L.l] = M;
     if (L.l < 8) {
-        const float a = L.l < 4 ? alpha[0] : alpha[1];
         const float pg = check::in(proj + L.t * 32 + L.l, 4, proj, proj_bytes, 1) ? proj[L.t * 32 + L.l] : 0.f;
-        const float s = sigmoid(a * pg / rv + bias[L.l]);
-        if (check::in(h + L.t * kNProj + L.l, 4, h, h_bytes, 3)) h[L.t * kNProj + L.l] = L.l < 4 ? s : 2.f * s;
+        const float g = gatemath::pre_post_gate(pg, rv, alpha, bias, L.l);
+        if (check::in(h + L.t * kNProj + L.l, 4, h, h_bytes, 3)) h[L.t * kNProj + L.l] = g;
     }
 }
 
@@ -164,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     const float a_res = alpha[2];
     const float pres = L.valid && check::in(proj + L.t * 32 + 8 + L.l, 4, proj, proj_bytes, 1)
                            ? proj[L.t * 32 + 8 + L.l] : 0.f;
-    const float M = sinkhorn(a_res * pres / rv + bias[8 + L.l], n_iter, Rs, Ms);
+    const float M = gatemath::sinkhorn(gatemath::res_logit(pres, rv, alpha, bias, L.l), n_iter, Rs, Ms, kThreads);
     // reverse mode on log-values, last iteration first (g = dL/dlog M):
     //   column step log M = log R - LSE_col:  g <- g - M sum_col(g)
     //   row step    log R = log A - LSE_row:  g <- g - R sum_row(g)
@@ -180,7 +113,7 @@ __global__ void __launch_bounds__(kThreads) gate_backward_kernel(
     if (L.l < 8 && L.valid) {
         a_g = L.l < 4 ? alpha[0] : alpha[1];
         pg = check::in(proj + L.t * 32 + L.l, 4, proj, proj_bytes, 1) ? proj[L.t * 32 + L.l] : 0.f;
-        const float s = sigmoid(a_g * pg / rv + bias[L.l]);
+        const float s = gatemath::sigmoid(a_g * pg / rv + bias[L.l]);
         const float gsc = L.l < 4 ? 1.f : 2.f;
         const float gh = check::in(grad_h + L.t * kNProj + L.l, 4, grad_h, h_bytes, 4) ? grad_h[L.t * kNProj + L.l] : 0.f;
         dl_g = gh * gsc * s * (1.f - s);

@@ -448,38 +448,61 @@ mhcpb_status_t mhcpb_forward_workspace_bytes(mhcpb_plan_t plan, size_t* bytes) {
     return MHCPB_OK;
 }
 
+// The forward, and with `gates` (non-null) the gate step fused into its
+// reduction.  Operands: 0 x, 1 w, 2 proj, 3 r, 4 workspace (16-byte aligned),
+// 5 alpha, 6 bias, 7 h (4-byte aligned, the gate calls' rule).
+struct FwdGates {
+    const float* alpha;
+    const float* bias;
+    int n_iter;
+    float* h;
+};
 static mhcpb_status_t forward_impl(mhcpb_plan_t plan, const void* x, const float* w, float eps,
                                    float* proj, float* r, void* workspace, size_t workspace_bytes,
-                                   void* stream, void* ev0, void* ev1, void* ev2) {
+                                   void* stream, void* ev0, void* ev1, void* ev2,
+                                   const FwdGates* gates) {
     if (plan == nullptr) return MHCPB_ERR_INVALID_ARG;
     const int64_t T = plan->T, K = plan->K;
     const size_t ws = fwd::workspace_bytes(T, K);
-    // an operand with no elements (at T = 0: all but W) needs no storage and
-    // its pointer is not checked
-    const void* all[5] = {x, w, proj, r, workspace};
-    const size_t all_sizes[5] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4),
-                                 (size_t)(T * fwd::kProjCols * 4), (size_t)(T * 4), ws};
-    const void* ptrs[5];
-    size_t sizes[5];
+    if (gates != nullptr && (gates->n_iter < 1 || gates->n_iter > MHCPB_GATE_MAX_ITER))
+        return MHCPB_ERR_UNSUPPORTED_SHAPE;
+    // an operand with no elements (at T = 0: all but W, alpha and bias) needs
+    // no storage and its pointer is not checked
+    const int n_all = gates != nullptr ? 8 : 5;
+    const void* all[8] = {x, w, proj, r, workspace, gates ? gates->alpha : nullptr,
+                          gates ? gates->bias : nullptr, gates ? gates->h : nullptr};
+    const size_t all_sizes[8] = {(size_t)(T * K * 2), (size_t)(kNProj * K * 4),
+                                 (size_t)(T * fwd::kProjCols * 4), (size_t)(T * 4), ws, 3 * 4, kNProj * 4,
+                                 (size_t)(T * kNProj * 4)};
+    const bool output[8] = {false, false, true, true, true, false, false, true};
+    const void* ptrs[8];
+    size_t sizes[8];
+    uintptr_t align[8];
+    bool is_out[8];
     int n = 0;
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < n_all; ++i) {
         if (all_sizes[i] == 0) continue;
         if (all[i] == nullptr) return MHCPB_ERR_INVALID_ARG;
         ptrs[n] = all[i];
+        align[n] = i < 5 ? 15u : 3u;
+        is_out[n] = output[i];
         sizes[n++] = all_sizes[i];
     }
     if (!(eps >= 0.f) || !(eps < INFINITY)) return MHCPB_ERR_INVALID_ARG;
     if (workspace_bytes < ws) return MHCPB_ERR_WORKSPACE_TOO_SMALL;
     for (int i = 0; i < n; ++i)
-        if ((reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != 0) return MHCPB_ERR_MISALIGNED;
-    Range rg[5];
+        if ((reinterpret_cast<uintptr_t>(ptrs[i]) & align[i]) != 0) return MHCPB_ERR_MISALIGNED;
+    Range rg[8];
     for (int i = 0; i < n; ++i) {
         rg[i].lo = reinterpret_cast<uintptr_t>(ptrs[i]);
         rg[i].hi = rg[i].lo + sizes[i];
     }
+    // outputs overlap nothing; of the inputs, X and W may not overlap either
+    // (the gates' alpha and bias, read-only, may)
     for (int i = 0; i < n; ++i)
         for (int j = i + 1; j < n; ++j)
-            if (overlap(rg[i], rg[j])) return MHCPB_ERR_ALIASING;
+            if ((is_out[i] || is_out[j] || (ptrs[i] == x && ptrs[j] == w)) && overlap(rg[i], rg[j]))
+                return MHCPB_ERR_ALIASING;
     for (int i = 0; i < n; ++i) {
         mhcpb_status_t s = check_device_ptr(ptrs[i], plan->device);
         if (s != MHCPB_OK) return s;
@@ -507,9 +530,11 @@ static mhcpb_status_t forward_impl(mhcpb_plan_t plan, const void* x, const float
     p.status = plan->d_status;
     p.timeout_ns = plan->timeout_ns;
     p.trace = plan->d_trace;
+    fwd::GateArgs ga{};
+    if (gates != nullptr) ga = fwd::GateArgs{gates->alpha, gates->bias, gates->n_iter, gates->h};
     cudaError_t e = fwd::launch(p, xm, wm, plan->fwd_grid, reinterpret_cast<cudaStream_t>(stream),
                                 reinterpret_cast<cudaEvent_t>(ev0), reinterpret_cast<cudaEvent_t>(ev1),
-                                reinterpret_cast<cudaEvent_t>(ev2));
+                                reinterpret_cast<cudaEvent_t>(ev2), gates != nullptr ? &ga : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "launch (forward kernels)");
     return MHCPB_OK;
 }
@@ -518,7 +543,7 @@ mhcpb_status_t mhcpb_forward(mhcpb_plan_t plan, const void* x, const float* w, f
                              float* proj, float* r, void* workspace, size_t workspace_bytes,
                              void* stream) {
     return forward_impl(plan, x, w, eps, proj, r, workspace, workspace_bytes, stream, nullptr,
-                        nullptr, nullptr);
+                        nullptr, nullptr, nullptr);
 }
 
 mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const float* w, float eps,
@@ -526,7 +551,16 @@ mhcpb_status_t mhcpb_forward_profiled(mhcpb_plan_t plan, const void* x, const fl
                                       size_t workspace_bytes, void* stream, void* ev_before,
                                       void* ev_between, void* ev_after) {
     return forward_impl(plan, x, w, eps, proj, r, workspace, workspace_bytes, stream, ev_before,
-                        ev_between, ev_after);
+                        ev_between, ev_after, nullptr);
+}
+
+mhcpb_status_t mhcpb_forward_gates(mhcpb_plan_t plan, const void* x, const float* w, float eps,
+                                   const float* alpha, const float* bias, int n_iter, float* proj,
+                                   float* r, float* h, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    const FwdGates gates{alpha, bias, n_iter, h};
+    return forward_impl(plan, x, w, eps, proj, r, workspace, workspace_bytes, stream, nullptr,
+                        nullptr, nullptr, &gates);
 }
 
 // Shared checks of the two gate calls: shape, pointers (device, alignment,

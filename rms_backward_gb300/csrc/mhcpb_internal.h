@@ -119,11 +119,21 @@ inline int grid_size(int64_t T, int64_t K, int sms) {
 size_t smem_bytes();
 cudaError_t setup();
 cudaError_t checked_site(uint32_t* site);
+// The gate step fused into the forward's reduction (mhcpb_forward_gates):
+// h [T, 24] from the proj and r the reduction writes.
+struct GateArgs {
+    const float* alpha;   // [3]
+    const float* bias;    // [24]
+    int n_iter;
+    float* h;             // [T, 24]
+};
 // launches both kernels on `stream`; x_map: X [T, K] BF16, boxes 64 x 128, 128-byte swizzle;
 // w_map: W [24, K] FP32, boxes 64 x 24, no swizzle; non-null events are
-// recorded before, between and after the two kernels
+// recorded before, between and after the two kernels; with `gates` the
+// reduction also writes the gates
 cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorMap& w_map, int grid,
-                   cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, cudaEvent_t ev2);
+                   cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, cudaEvent_t ev2,
+                   const GateArgs* gates = nullptr);
 }  // namespace fwd
 
 // Gate/normalisation step (mhcpb_gate_forward / mhcpb_gate_backward): a

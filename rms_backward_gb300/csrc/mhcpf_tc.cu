@@ -43,6 +43,7 @@
 // partial lines from L2.  Every mbarrier wait is bounded (wait_bar).
 #include <cuda_bf16.h>
 
+#include "mhcg_math.cuh"
 #include "mhcpb_check.cuh"
 #include "mhcpb_internal.h"
 #include "mhcpb_wait.cuh"
@@ -480,10 +481,11 @@ __device__ __forceinline__ float sum_chunks(const float* src, int64_t stride, in
     return a;
 }
 
+template <bool GATES>
 __global__ void __launch_bounds__(kLineThreads)
     fwd_reduce_lines_kernel(const float* __restrict__ part, float* __restrict__ proj,
                             float* __restrict__ r, int T, int t_pad, int n_fc, float kf, float eps,
-                            int discard) {
+                            int discard, GateArgs g) {
     __shared__ float sums[kPartRows][kLineTokens + 1];
     ptx::grid_launch_dependents();   // the next forward's kernel 1 may be scheduled
     ptx::grid_dependency_wait();
@@ -518,6 +520,29 @@ __global__ void __launch_bounds__(kLineThreads)
         const int t = t0 + tt;
         if (t < T && check::in(r + t, 4, r, (size_t)T * 4, 3))
             r[t] = sqrtf(sums[kNProj][tt] / kf + eps);   // the mean of the squares, eps, root
+    }
+    if (GATES && threadIdx.x < kLineTokens * 16) {
+        // the gate step on the values just stored: a half-warp per token,
+        // token pairs per warp as in the gate kernels, and a token past T
+        // given the gate kernels' inputs for it (r = 1, projections 0), so
+        // every warp-wide choice and so every bit is the same as
+        // mhcpb_gate_forward on the stored proj and r
+        const int tt = threadIdx.x >> 4, l = threadIdx.x & 15;
+        const int t = t0 + tt;
+        const bool valid = t < T;
+        const float rv = valid ? sqrtf(sums[kNProj][tt] / kf + eps) : 1.f;
+        const float pres = valid ? sums[8 + l][tt] : 0.f;
+        const float M = gatemath::sinkhorn(gatemath::res_logit(pres, rv, g.alpha, g.bias, l), g.n_iter, nullptr,
+                                           nullptr, 0);
+        if (valid) {
+            const size_t h_bytes = (size_t)T * kNProj * 4;   // checked builds
+            float* ht = g.h + (size_t)t * kNProj;
+            if (check::in(ht + 8 + l, 4, g.h, h_bytes, 5)) ht[8 + l] = M;
+            if (l < 8) {
+                const float gv = gatemath::pre_post_gate(sums[l][tt], rv, g.alpha, g.bias, l);
+                if (check::in(ht + l, 4, g.h, h_bytes, 5)) ht[l] = gv;
+            }
+        }
     }
 }
 
@@ -569,7 +594,8 @@ cudaError_t setup() {
 }
 
 cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorMap& w_map, int grid,
-                   cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, cudaEvent_t ev2) {
+                   cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1, cudaEvent_t ev2,
+                   const GateArgs* gates) {
     cudaError_t e;
     if (ev0 && (e = cudaEventRecord(ev0, stream)) != cudaSuccess) return e;
     {
@@ -590,8 +616,10 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorM
     // discard needs 128-byte lines: t_pad is a multiple of 32 floats
     const int discard = (reinterpret_cast<uintptr_t>(p.partial) & 127u) == 0 ? 1 : 0;
     // one wave of line blocks (kernel 1's grid is the SM count unless the
-    // problem has fewer units, or a cap lowers it), else the output threads
-    const bool lines = p.t_pad / kLineTokens <= grid;
+    // problem has fewer units, or a cap lowers it), else the output threads;
+    // the gates need a token's sums together: always lines
+    const bool lines = gates != nullptr || p.t_pad / kLineTokens <= grid;
+    const GateArgs g = gates != nullptr ? *gates : GateArgs{nullptr, nullptr, 0, nullptr};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = lines ? dim3((unsigned)(p.t_pad / kLineTokens))
                         : dim3((unsigned)(((int64_t)kPartRows * p.t_pad + kOutThreads - 1) / kOutThreads));
@@ -603,10 +631,17 @@ cudaError_t launch(const FwdParams& p, const CUtensorMap& x_map, const CUtensorM
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, lines ? fwd_reduce_lines_kernel : fwd_reduce_outputs_kernel,
-                                static_cast<const float*>(p.partial), p.proj, p.r, p.T, p.t_pad,
-                                p.n_fc, (float)p.K, p.eps, discard)) != cudaSuccess)
-        return e;
+    const float* part = p.partial;
+    if (gates != nullptr)
+        e = cudaLaunchKernelEx(&cfg, fwd_reduce_lines_kernel<true>, part, p.proj, p.r, p.T, p.t_pad, p.n_fc,
+                               (float)p.K, p.eps, discard, g);
+    else if (lines)
+        e = cudaLaunchKernelEx(&cfg, fwd_reduce_lines_kernel<false>, part, p.proj, p.r, p.T, p.t_pad, p.n_fc,
+                               (float)p.K, p.eps, discard, g);
+    else
+        e = cudaLaunchKernelEx(&cfg, fwd_reduce_outputs_kernel, part, p.proj, p.r, p.T, p.t_pad, p.n_fc,
+                               (float)p.K, p.eps, discard);
+    if (e != cudaSuccess) return e;
     if (ev2 && (e = cudaEventRecord(ev2, stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }

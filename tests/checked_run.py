@@ -114,6 +114,20 @@ def forward():
             ok, st = F.check_proj(proj.cpu().numpy(), ref_p, bound)
             okr, str_ = F.check_r(r.cpu().numpy(), ref_r)
             assert ok and okr, f"forward T={T} cap={cap}: {st} {str_}"
+        # the gate step fused into the reduction: the same bits as the gate call on proj and r
+        plan = Plan(T, K, 0)
+        alpha = torch.tensor([1.0, 0.75, 1.25], device=DEV)
+        bias = torch.linspace(-0.5, 0.5, 24, device=DEV)
+        p1, r1, h1 = (torch.empty(s_, device=DEV) for s_ in ((T, 32), (T,), (T, 24)))
+        h2 = torch.empty((T, 24), device=DEV)
+        ws = torch.empty(plan.forward_workspace_bytes, dtype=torch.uint8, device=DEV)
+        plan.forward_gates(x, w, alpha, bias, p1, r1, h1, ws)
+        mhc_gate_forward(p1, r1, alpha, bias, h2)
+        torch.cuda.synchronize()
+        assert plan.device_status() == 0
+        plan.close()
+        no_sites(f"forward with gates T={T} K={K}")
+        assert torch.equal(h1.view(torch.int32), h2.view(torch.int32)), f"fused gates T={T}"
 
 
 def gates():
