@@ -453,7 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 //  * lines (at most one block per SM): block = 32 tokens, warp j' sums
 //    partial row j' (lane = token, each load one 128-byte line), and the sums
 //    leave through shared memory as whole proj rows (a token's 32 floats are
-//    one 128-byte line).  68 registers x 800 threads: one block per SM;
+//    one 128-byte line).  64 registers x 800 threads: one block per SM.  With
+//    the gate step fused in (mhcpb_forward_gates) it also runs the gates on
+//    the sums, and is then taken at every T;
 //  * outputs (more blocks than SMs): thread = (row j', token t), 256-thread
 //    blocks, several per SM.  Its warps write 4-byte pieces of 32 proj rows
 //    each, which costs ~1.7 us per call at T = 4096; but it keeps more loads
