@@ -63,7 +63,7 @@ typedef enum {
     MHCPB_OK = 0,
     MHCPB_ERR_INVALID_ARG = 1,        /* NULL plan/pointer, addend presence disagreeing with the plan */
     MHCPB_ERR_UNSUPPORTED_SHAPE = 2,  /* T < 0, K not a positive multiple of 8, or above the maxima below */
-    MHCPB_ERR_MISALIGNED = 3,         /* a pointer not 16-byte aligned */
+    MHCPB_ERR_MISALIGNED = 3,         /* a pointer not 16-byte aligned (4-byte for the gate operands) */
     MHCPB_ERR_ALIASING = 4,           /* two operands (or workspace) share bytes */
     MHCPB_ERR_WRONG_DEVICE = 5,       /* a pointer not in device memory of the plan's device */
     MHCPB_ERR_TF32_NOT_ALLOWED = 6,   /* flags lack MHCPB_ALLOW_TF32 */
