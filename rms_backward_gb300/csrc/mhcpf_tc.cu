@@ -277,9 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and as the swizzled BF16 hi/lo operand.  Warp 2 converts the even
         // boxes, warp 3 the odd ones, each box read whole into registers before
         // it is overwritten.  Chunk 0 was fetched by thread 0 before the
-        // block-wide sync, chunk 1 is fetched now, chunk m + 1 (m >= 1) once the
-        // MMAs of chunk m - 1 have left its slot; so a chunk is converted while
-        // the MMAs still work on the previous one.
+        // block-wide sync, chunk 1 is fetched once chunk 0 is converted, chunk
+        // m + 1 (m >= 1) once the MMAs of chunk m - 1 have left its slot; so a
+        // chunk is converted while the MMAs still work on the previous one.
         const bool fetcher = warp == 2 && lane == 0;
         const int wq = warp - 2;   // boxes wq, wq + 2, ...
         int n_chunks = 0, fc_first = 0;
@@ -288,10 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             n_chunks = unit_at(p, u_end - 1).fc - fc_first + 1;   // units are chunk-major
         }
         int n_raw = n_chunks > 0 ? 1 : 0;
-        if (fetcher && n_chunks > 1) {
-            fetch_raw_w(fc_first + 1, 1);
-            n_raw = 2;
-        }
         bool ok = true;
         int m = 0;
         for (; m < n_chunks && ok; ++m) {
@@ -337,6 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) ptx::mbar_arrive(bar(B_WF + slot * kBoxes + b));
             }
             if (fetcher) FTRACE(F_W_READY, m);
+            // chunk 1 is fetched only once chunk 0 is converted, not at the
+            // start: then the first X boxes land without it in the way (at
+            // K = 20480, T = 4096 the call is ~0.35 us faster)
+            if (fetcher && m == 0 && n_chunks > 1) {
+                fetch_raw_w(fc_first + 1, 1);
+                n_raw = 2;
+            }
             // chunk m + 1 goes to slot (m + 1) % 2 once the MMAs of chunk m - 1
             // (which also proves that chunk's conversion finished) have left it
             if (fetcher && m >= 1 && m + 1 < n_chunks) {
