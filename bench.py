@@ -508,13 +508,63 @@ def _long_side(lib_abi, flush, stream, peak, reps=50):
         flush.fill_(1.0)
         step()
     st = _stats_us(_step_times(step, flush, reps, "flushed", stream))
+    chain = _sublayer_chain(plan, x, w, r, dx, dw, ws, flush, stream, reps)
     if plan.device_status() != 0:
         raise RuntimeError("device-side timeout at the long sublayer")
     plan.close()
     alg = WL.algorithmic_bytes(T, K)
     gbs = alg / (st["median_us"] * 1e-6) / 1e9
     return dict(st, T=T, K=K, value=gbs, unit="GB/s", pct_of_hbm_peak=100.0 * gbs / peak,
-                how=_l2_note("flushed", 2 * T * K, None))
+                how=_l2_note("flushed", 2 * T * K, None), chain=chain)
+
+
+def _sublayer_chain(plan, x, w, r, dx, dw, ws, flush, stream, reps):
+    """The parts of an mHC sublayer's forward and backward this library
+    covers, in order, at the long sublayer: the forward with the gates fused
+    in, the gate backward, then this stage's backward fed by it.  Flushed
+    medians of the chain and of each part alone.  Context beside the pages'
+    per-sublayer figure at 16k tokens, which covers more (the stream collapse
+    and the rest of the layer)."""
+    import torch
+    from rms_backward_gb300 import mhc_gate_backward
+    T, K = plan.T, plan.K
+    dev = x.device
+    rng = np.random.default_rng(1)
+    alpha = torch.from_numpy(rng.uniform(0.5, 1.5, 3).astype(np.float32)).to(dev)
+    bias = torch.from_numpy(rng.normal(0, 0.5, 24).astype(np.float32)).to(dev)
+    gh = torch.from_numpy(rng.normal(0, 1e-2, (T, 24)).astype(np.float32)).to(dev)
+    proj = torch.empty((T, 32), dtype=torch.float32, device=dev)
+    rr = torch.empty((T,), dtype=torch.float32, device=dev)
+    h = torch.empty((T, 24), dtype=torch.float32, device=dev)
+    gp = torch.empty((T, 32), dtype=torch.float32, device=dev)
+    gr = torch.empty((T,), dtype=torch.float32, device=dev)
+    fws = torch.empty(plan.forward_workspace_bytes, dtype=torch.uint8, device=dev)
+    sh = stream.cuda_stream
+
+    def fwd():
+        plan.forward_gates(x, w, alpha, bias, proj, rr, h, fws, stream=sh)
+
+    def gbwd():
+        mhc_gate_backward(proj, rr, alpha, bias, gh, gp, gr, stream=sh)
+
+    def bwd():
+        plan.execute(x, w, gp, gr, rr, dx, dw, ws, stream=sh)
+
+    def chain():
+        fwd()
+        gbwd()
+        bwd()
+
+    for _ in range(3):
+        flush.fill_(1.0)
+        chain()
+    out = {"total": _stats_us(_step_times(chain, flush, reps, "flushed", stream))}
+    for name, fn in (("forward_gates", fwd), ("gate_backward", gbwd), ("backward", bwd)):
+        out[name + "_median_us"] = _stats_us(_step_times(fn, flush, reps, "flushed", stream))["median_us"]
+    out["how"] = ("mhcpb_forward_gates, mhcpb_gate_backward, mhcpb_execute in sequence at T=16384, "
+                  "K=20480, 20 Sinkhorn iterations, L2 flushed before each chain or part; the parts "
+                  "of an mHC sublayer this library covers, not the whole sublayer")
+    return out
 
 
 def _cpu_worker(spec):
