@@ -225,8 +225,9 @@ mhcpb_status_t mhcpb_plan_query(mhcpb_plan_t plan, int which, int64_t* value);
  * sites[5] = {tensor-core backward, FMA backward, dW reduction, forward, gate
  * kernels}, each 0 (none since the last call) or 1 + the site within that
  * family's source.  *checked is 1 for a checked build; a normal build sets
- * it to 0 and every site to 0, makes no CUDA call and cannot fail.  The
- * words are per device (the current one) and shared by all plans. */
+ * it to 0 and every site to 0 and makes no CUDA call.  NULL arguments:
+ * MHCPB_ERR_INVALID_ARG.  The words are per device (the current one) and
+ * shared by all plans. */
 mhcpb_status_t mhcpb_debug_checked_sites(uint32_t* sites, int* checked);
 
 /* Sets the bound on every wait inside the plan's kernels (default 1 s,
