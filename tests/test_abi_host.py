@@ -195,3 +195,14 @@ def test_binding_constants_match_the_header():
     m = re.search(r"#define\s+MHCPB_PARTIAL_TOKENS\(T\)\s+(\d+)", open(HEADER).read())
     for T in (1, 512, 4096, 1 << 24):
         assert abi.MHCPB_PARTIAL_TOKENS(T) == int(m.group(1))
+
+
+def test_checked_sites_in_a_normal_build(lib):
+    """A normal build reports itself unchecked with every site 0, without any
+    CUDA call (so it works here, with no GPU); NULL arguments are rejected."""
+    checked, sites = abi.mhcpb_debug_checked_sites()
+    assert checked is False and set(sites.values()) == {0} and len(sites) == 5
+    import ctypes
+    assert lib.mhcpb_debug_checked_sites(None, None) == abi.MHCPB_ERR_INVALID_ARG
+    one = ctypes.c_int()
+    assert lib.mhcpb_debug_checked_sites(None, ctypes.byref(one)) == abi.MHCPB_ERR_INVALID_ARG
